@@ -1,0 +1,599 @@
+#!/usr/bin/env python
+"""Throughput of the speculative-decoding verify step on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one full verify call (every kernel of the path) over one batch of
+synthetic logits already resident in HBM.  The default workload is the
+SmolLM2-shaped chain verify (B=64, γ=5, V=49152 bf16, T=0.8, top_p=0.9);
+--workload selects another of the pages' settings.  Rank 0 prints one JSON
+line.  Under torchrun every rank verifies its own batch (weak scaling, no
+data-path collective); timing is the max over ranks.
+
+The timed region replays the K steps from a CUDA graph (no host launch gaps)
+and rotates over enough copies of the inputs that they exceed 4x the L2
+cache, so every step reads its logits from HBM.  A second, instrumented
+replay records CUDA events around each kernel (on the kernels' stream) to
+time the dominant kernel for the roofline.  "e2e" is the same metric through
+the public Python call with the step's inputs copied from pinned host memory
+and its outputs copied back, every step.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_HBM_GBS = 6800.0
+WORKLOADS = {
+    "tiny": synth.TINY,
+    "smollm2": synth.SMOLLM2,
+    "llama3-greedy": synth.LLAMA3_GREEDY,
+    "llama3-sample": synth.LLAMA3_SAMPLE,
+    "qwen3-d2t": synth.QWEN3_D2T,
+    "tree": synth.TREE,
+}
+DEFAULT_WORKLOAD = "smollm2"
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="CPU budget of the oracle baseline sample")
+    ap.add_argument("--reference-seconds", type=float, default=150.0,
+                    help="wall budget of the whole --impl reference run")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args(argv)
+
+
+# ------------------------------------------------------------ distributed ----
+
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+
+    def init(self, device_ok: bool):
+        if self.world > 1:
+            import torch.distributed as dist
+            dist.init_process_group("nccl" if device_ok else "gloo")
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        return self._reduce(x, "max")
+
+    def sum(self, x: float) -> float:
+        return self._reduce(x, "sum")
+
+    def _reduce(self, x: float, op: str) -> float:
+        if not self.pg:
+            return x
+        import torch
+        dev = torch.device("cuda", self.local_rank) if torch.cuda.is_available() else torch.device("cpu")
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX if op == "max" else self.pg.ReduceOp.SUM)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+def aggregate(times_ms: list[float], units: list[float]) -> tuple[float, float]:
+    """Whole-job throughput from per-rank (elapsed ms, units): units summed,
+    time = the slowest rank.  Returns (units per second, max ms)."""
+    t = max(times_ms)
+    return sum(units) / (t / 1e3), t
+
+
+# ------------------------------------------------------------------ peaks ----
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def ncu_traffic(workload: str, kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    summary is missing or was taken on different kernel sources."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.md")
+    try:
+        lines = open(path).read().splitlines()
+    except OSError:
+        return None
+    src = source_hash()
+    for ln in lines:
+        cells = [c.strip() for c in ln.strip().strip("|").split("|")]
+        if len(cells) >= 4 and cells[0] == workload and cells[1] == kernel:
+            try:
+                traffic, h = float(cells[2]), cells[3]
+            except ValueError:
+                continue
+            return traffic if h == src else None
+    return None
+
+
+def source_hash() -> str:
+    d = os.path.join(ROOT, "draft_token_verification_sv_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(d)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            h.update(name.encode())
+            h.update(open(os.path.join(d, name), "rb").read())
+    return h.hexdigest()[:12]
+
+
+# ----------------------------------------------------------------- clocks ----
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str | None):
+        self.uuid = uuid
+        self.proc = None
+        self.out = None
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100"]
+        if self.uuid:
+            cmd += ["-i", self.uuid]
+        try:
+            self.out = tempfile.TemporaryFile(mode="w+")
+            self.proc = subprocess.Popen(cmd, stdout=self.out, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict | None:
+        if not self.proc:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            self.proc.wait()
+        self.out.seek(0)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.out.read().splitlines():
+            cells = [c.strip() for c in ln.split(",")]
+            if len(cells) < 7:
+                continue
+            try:
+                sm.append(float(cells[0]))
+                mx.append(float(cells[1]))
+            except ValueError:
+                continue
+            for n, c in zip(names, cells[3:7]):
+                if c.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------- workloads ----
+
+def make_inputs(cfg, dev, sv):
+    """Seeded inputs on the device, plus draft ids drawn by the library's
+    draft sampler from the uniforms (outside any timed region)."""
+    import torch
+    if isinstance(cfg, synth.TreeConfig):
+        x = synth.make_tree_inputs(cfg)
+        store = x["logits_store"]
+        logits = torch.from_numpy(store.view(np.int16)).view(torch.bfloat16) if cfg.dtype == "bf16" \
+            else torch.from_numpy(store)
+        return dict(host=x, logits=logits.to(dev), parents=torch.from_numpy(x["parents"]).to(dev),
+                    tokens=torch.from_numpy(x["tokens"]).to(dev))
+    x = synth.make_chain_inputs(cfg)
+
+    def as_t(store):
+        if cfg.dtype == "bf16":
+            return torch.from_numpy(np.ascontiguousarray(store).view(np.int16)).view(torch.bfloat16).to(dev)
+        return torch.from_numpy(np.ascontiguousarray(store)).to(dev)
+
+    target, draft = as_t(x["target_store"]), as_t(x["draft_store"])
+    B, G = x["batch"], x["gamma"]
+    u_draft = torch.from_numpy(x["u_draft"]).to(dev)
+    tok, _ = sv.sample(draft.reshape(B * G, -1), cfg.temperature, cfg.top_p,
+                       u_draft.reshape(-1) if cfg.temperature > 0 else None)
+    d2t = t2d = None
+    if x["d2t"] is not None:
+        d2t = torch.from_numpy(x["d2t"]).to(dev)
+        t2d = sv.build_t2d(d2t, x["vocab"])[0]
+        tok = d2t[tok.long()]
+    ids = tok.reshape(B, G).to(torch.int32).contiguous()
+    torch.cuda.synchronize()
+    x["draft_ids"] = ids.cpu().numpy()
+    return dict(host=x, target=target, draft=draft, ids=ids, d2t=d2t, t2d=t2d,
+                u_accept=torch.from_numpy(x["u_accept"]).to(dev),
+                u_resample=torch.from_numpy(x["u_resample"]).to(dev))
+
+
+def step_bytes(cfg) -> int:
+    return cfg.algorithmic_bytes()
+
+
+class Runner:
+    """Pre-marshalled C-ABI calls, one per rotating input set."""
+
+    def __init__(self, sv, cfg, inputs, nsets, dev):
+        import torch
+        from draft_token_verification_sv_gb300 import _native as N
+        from draft_token_verification_sv_gb300.verify import chain_desc
+        self.N = N
+        self.lib = N.lib()
+        self.cfg = cfg
+        self.tree = isinstance(cfg, synth.TreeConfig)
+        self.sets = []
+        self.keep = []
+        vp = lambda t: ctypes.c_void_p(t.data_ptr()) if t is not None else None
+        if self.tree:
+            B, Nn = cfg.batch, cfg.nodes
+            d = N.TreeDesc()
+            d.batch, d.nodes, d.vocab, d.max_depth = B, Nn, cfg.vocab, cfg.max_depth
+            d.dtype = N.SV_BF16 if cfg.dtype == "bf16" else N.SV_F32
+            d.row_stride = cfg.vocab
+            self.desc = d
+            ws_need = self.lib.sv_tree_workspace_size(ctypes.byref(d))
+        else:
+            d = chain_desc(inputs["target"], inputs["draft"], cfg.temperature, cfg.top_p, inputs["d2t"])
+            self.desc = d
+            ws_need = self.lib.sv_chain_workspace_size(ctypes.byref(d))
+        self.ws = torch.zeros(ws_need, dtype=torch.uint8, device=dev)
+        L = cfg.max_depth + 1 if self.tree else cfg.gamma + 1
+        B = cfg.batch
+        self.out = dict(tokens=torch.empty((B, L), dtype=torch.int32, device=dev),
+                        k=torch.empty(B, dtype=torch.int32, device=dev),
+                        status=torch.empty(B, dtype=torch.int32, device=dev),
+                        path=torch.empty((B, L), dtype=torch.int32, device=dev))
+        o = self.out
+        for s in range(nsets):
+            if self.tree:
+                lg = inputs["logits"] if s == 0 else inputs["logits"].clone()
+                self.keep.append(lg)
+                args = (ctypes.byref(self.desc), vp(lg), vp(inputs["parents"]), vp(inputs["tokens"]),
+                        vp(o["k"]), vp(o["path"]), vp(o["tokens"]), vp(o["status"]), vp(self.ws),
+                        ctypes.c_size_t(self.ws.numel()))
+            else:
+                tg = inputs["target"] if s == 0 else inputs["target"].clone()
+                dr = None
+                if cfg.temperature > 0:
+                    dr = inputs["draft"] if s == 0 else inputs["draft"].clone()
+                self.keep += [tg, dr]
+                args = (ctypes.byref(self.desc), vp(tg), vp(dr), vp(inputs["d2t"]), vp(inputs["t2d"]),
+                        vp(inputs["ids"]), vp(inputs["u_accept"]), vp(inputs["u_resample"]),
+                        vp(o["tokens"]), vp(o["k"]), None, None, vp(o["status"]), vp(self.ws),
+                        ctypes.c_size_t(self.ws.numel()))
+            self.sets.append(args)
+        self.fn = self.lib.sv_verify_tree if self.tree else self.lib.sv_verify_chain
+
+    def step(self, s: int, stream_handle):
+        st = self.fn(*self.sets[s % len(self.sets)], stream_handle)
+        if st != 0:
+            raise RuntimeError(f"verify call failed with status {st}")
+
+
+def n_sets_for(cfg) -> int:
+    per = step_bytes(cfg)
+    return max(2, math.ceil(4 * L2_BYTES / per))
+
+
+# ------------------------------------------------------------- our arm ----
+
+def run_ours(args, dist: Dist):
+    import torch
+    import draft_token_verification_sv_gb300 as sv
+    from draft_token_verification_sv_gb300 import build as b
+    b.build()
+    assert torch.cuda.is_available(), "bench needs a CUDA device"
+    dev = torch.device("cuda", dist.local_rank)
+    torch.cuda.set_device(dev)
+    dist.init(True)
+    cfg = WORKLOADS[args.workload]
+    inputs = make_inputs(cfg, dev, sv)
+    nsets = n_sets_for(cfg)
+    R = Runner(sv, cfg, inputs, nsets, dev)
+    lib = R.lib
+    stream = torch.cuda.Stream(device=dev)
+    sh = ctypes.c_void_p(stream.cuda_stream)
+    K, W = args.steps, args.warmup
+
+    # Warm-up (also sets kernel attributes before any capture).
+    with torch.cuda.stream(stream):
+        for s in range(max(W, 3)):
+            R.step(s, sh)
+    stream.synchronize()
+
+    # Pure graph of K steps.
+    launches0 = lib.sv_launch_count()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for s in range(K):
+            R.step(s, sh)
+    launches = int(lib.sv_launch_count() - launches0)
+    per_step_launches = launches // K
+
+    # Instrumented graph: events around every kernel of every step.
+    nph = per_step_launches + 1
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(nph)] for _ in range(K)]
+    with torch.cuda.stream(stream):
+        for row in events:
+            for e in row:
+                e.record(stream)
+    stream.synchronize()
+    handles = [(ctypes.c_void_p * nph)(*[ctypes.c_void_p(e.cuda_event) for e in row]) for row in events]
+    gi = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gi, stream=stream):
+        for s in range(K):
+            lib.sv_set_phase_events(handles[s], nph)
+            R.step(s, sh)
+
+    # Clock samples over a load window that ends with the timed region.
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+        uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    except Exception:
+        uuid = None
+    sampler = ClockSampler(uuid)
+    sampler.start()
+    t_end = time.time() + 1.5
+    with torch.cuda.stream(stream):
+        while time.time() < t_end:
+            g.replay()
+            stream.synchronize()
+
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    dist.barrier()
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        g.replay()
+        end.record(stream)
+    torch.cuda.synchronize()
+    dist.barrier()
+    clocks = sampler.stop()
+    elapsed = start.elapsed_time(end)
+
+    # Instrumented replay: per-kernel durations.
+    with torch.cuda.stream(stream):
+        gi.replay()
+    torch.cuda.synchronize()
+    phase_ms = [[row[i].elapsed_time(row[i + 1]) for i in range(nph - 1)] for row in events]
+    avg_phase = [statistics.mean(p[i] for p in phase_ms) for i in range(nph - 1)]
+
+    units = cfg.rows_metric * K
+    t_max = dist.max(elapsed)
+    tot_units = dist.sum(units)
+    value = tot_units / (t_max / 1e3)
+
+    # End to end through the public call, pinned host inputs each step.
+    e2e = run_e2e(cfg, inputs, sv, dev, stream, K, dist)
+
+    peak, peak_kind = hbm_peak()
+    dom = 0
+    dom_name = {True: "greedy_kernel(tree)", False: None}[R.tree]
+    if not R.tree:
+        dom_name = "greedy_kernel(chain)" if cfg.temperature == 0 else (
+            "stats_resident_kernel" if cfg.top_p < 1 else "stats_stream_kernel")
+    achieved = step_bytes(cfg) / (avg_phase[dom] / 1e3) / 1e9
+    traffic = ncu_traffic(args.workload, dom_name)
+    res = {
+        "metric": "verify rows/s (B*(2*gamma+1) rows per chain step, B*N per tree step)",
+        "value": value,
+        "unit": "rows/s",
+        "n_gpus": dist.world,
+        "steps": K,
+        "warmup": W,
+        "ms_per_step": t_max / K,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16" if cfg.dtype == "bf16" else "f32",
+        "data": "synthetic (seeded, shapes and value recipe of the pages' settings)",
+        "config": config_of(cfg, args.workload, nsets, dist.world),
+        "hbm_gbs_algorithmic": step_bytes(cfg) * K / (elapsed / 1e3) / 1e9,
+        "roofline": {"bound": "hbm", "kernel": dom_name, "achieved": achieved, "peak": peak,
+                     "peak_source": f"hbm_gbs of {peak_kind}", "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": traffic, "bytes_per_launch": step_bytes(cfg),
+                     "avg_launch_ms": avg_phase[dom]},
+        "phase_ms": avg_phase,
+        "gpu_launches": launches,
+        "e2e": e2e,
+        "clocks": clocks,
+    }
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(cfg, inputs, args.cpu_seconds)
+    dist.close()
+    return res
+
+
+def config_of(cfg, workload, nsets, world):
+    c = {"workload": workload, "batch": cfg.batch, "vocab": cfg.vocab, "dtype": cfg.dtype,
+         "l2": f"{nsets} rotating input copies ({nsets * step_bytes(cfg) / 1e6:.0f} MB > 4x L2)",
+         "parallelism": f"replicas x{world} (batch rows independent)"}
+    if isinstance(cfg, synth.TreeConfig):
+        c.update(nodes=cfg.nodes, max_depth=cfg.max_depth, temperature=0.0)
+    else:
+        c.update(gamma=cfg.gamma, temperature=cfg.temperature, top_p=cfg.top_p,
+                 draft_vocab=cfg.draft_vocab or cfg.vocab)
+    return c
+
+
+def run_e2e(cfg, inputs, sv, dev, stream, K, dist):
+    import torch
+    tree = isinstance(cfg, synth.TreeConfig)
+    names = ["logits", "parents", "tokens"] if tree else \
+        ["target", "draft", "ids", "u_accept", "u_resample"]
+    if not tree and cfg.temperature == 0:
+        names = ["target", "ids"]
+    host = {n: inputs[n].cpu().pin_memory() for n in names}
+    devb = {n: torch.empty_like(inputs[n]) for n in names}
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    L = cfg.max_depth + 1 if tree else cfg.gamma + 1
+    out_host = torch.empty((cfg.batch, L), dtype=torch.int32).pin_memory()
+    k_host = torch.empty(cfg.batch, dtype=torch.int32).pin_memory()
+    d2h = out_host.numel() * 4 + k_host.numel() * 4
+
+    def one():
+        for n in names:
+            devb[n].copy_(host[n], non_blocking=True)
+        if tree:
+            o = sv.verify_tree(devb["logits"], devb["parents"], devb["tokens"], cfg.max_depth)
+            out_host.copy_(o["out_tokens"], non_blocking=True)
+            k_host.copy_(o["accept_len"], non_blocking=True)
+        else:
+            o = sv.verify_chain(devb["target"], devb.get("draft"), devb["ids"], devb.get("u_accept"),
+                                devb.get("u_resample"), cfg.temperature, cfg.top_p, d2t=inputs["d2t"],
+                                t2d=inputs["t2d"], probs=False)
+            out_host.copy_(o["tokens"], non_blocking=True)
+            k_host.copy_(o["num_accepted"], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            one()
+        stream.synchronize()
+        dist.barrier()
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for _ in range(K):
+            one()
+        end.record(stream)
+    torch.cuda.synchronize()
+    dist.barrier()
+    ms = dist.max(start.elapsed_time(end))
+    units = dist.sum(cfg.rows_metric * K)
+    return {"value": units / (ms / 1e3), "unit": "rows/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms / K}
+
+
+# ------------------------------------------------------ oracle baselines ----
+
+def oracle_rows(cfg, host, rows):
+    from oracle import sv_oracle as O
+    if isinstance(cfg, synth.TreeConfig):
+        return O.verify_tree(host["logits"], host["parents"], host["tokens"], host["max_depth"], rows=rows)
+    return O.verify_chain(host["target"], host["draft"] if cfg.temperature > 0 else None,
+                          host["draft_ids"], host["u_accept"], host["u_resample"], cfg.temperature,
+                          cfg.top_p, d2t=host["d2t"], rows=rows)
+
+
+def units_per_batch_row(cfg) -> int:
+    return cfg.nodes if isinstance(cfg, synth.TreeConfig) else 2 * cfg.gamma + 1
+
+
+def cpu_baseline(cfg, inputs, seconds):
+    """The fp64 oracle as it stands, single-threaded, on batch rows of the
+    same workload until the CPU budget is spent (at least one row)."""
+    host = inputs["host"]
+    B = cfg.batch
+    done = 0
+    t0 = time.perf_counter()
+    while done < B and (done == 0 or time.perf_counter() - t0 < seconds):
+        oracle_rows(cfg, host, [done])
+        done += 1
+    dt = time.perf_counter() - t0
+    return {"value": done * units_per_batch_row(cfg) / dt, "unit": "rows/s", "cores": 1, "kind": "oracle",
+            "sample": f"{done} of {B} batch rows of the {cfg.name} workload, fp64 numpy, one thread"}
+
+
+def oracle_draft_ids(cfg, host, rows):
+    """Draft ids of the given batch rows, drawn by the oracle from q with the
+    seeded uniforms (argmax at T = 0)."""
+    from oracle import sv_oracle as O
+    G = host["gamma"]
+    ids = host.setdefault("draft_ids", np.zeros((host["batch"], G), np.int32))
+    d2t = host["d2t"]
+    for b in rows:
+        for i in range(G):
+            tok, _ = O.sample_row(host["draft"][b, i], cfg.temperature, cfg.top_p,
+                                  float(host["u_draft"][b, i]), tie_index=d2t)
+            ids[b, i] = d2t[tok] if d2t is not None else tok
+
+
+def run_reference(args, dist: Dist):
+    """The oracle timed as the reference arm: K steps, each a bounded sample
+    of batch rows of the same workload."""
+    cfg = WORKLOADS[args.workload]
+    chain = not isinstance(cfg, synth.TreeConfig)
+    host = synth.make_chain_inputs(cfg) if chain else synth.make_tree_inputs(cfg)
+    if chain:
+        oracle_draft_ids(cfg, host, [0])
+    t0 = time.perf_counter()
+    oracle_rows(cfg, host, [0])
+    t_row = max(time.perf_counter() - t0, 1e-3)
+    K, W = args.steps, args.warmup
+    per_step = max(1, min(cfg.batch, int(args.reference_seconds / (K + W) / t_row)))
+    rows = list(range(per_step))
+    if chain:
+        oracle_draft_ids(cfg, host, rows[1:])
+    for _ in range(W):
+        oracle_rows(cfg, host, rows[:1])
+    times = []
+    for _ in range(K):
+        t = time.perf_counter()
+        oracle_rows(cfg, host, rows)
+        times.append(time.perf_counter() - t)
+    total = sum(times)
+    value = K * per_step * units_per_batch_row(cfg) / total
+    return {"impl": "reference", "metric": "verify rows/s (B*(2*gamma+1) rows per chain step, B*N per tree step)",
+            "value": value, "unit": "rows/s", "n_gpus": dist.world, "steps": K, "warmup": W,
+            "ms_per_step": 1e3 * total / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic (seeded)", "config": config_of(cfg, args.workload, 1, 1),
+            "cpu_baseline": {"value": value, "unit": "rows/s", "cores": 1, "kind": "oracle",
+                             "sample": f"{per_step} batch rows of the {cfg.name} workload per step"},
+            "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    dist = Dist()
+    if args.impl == "reference":
+        if dist.rank != 0:
+            return 0
+        print(json.dumps(run_reference(args, dist)), flush=True)
+        return 0
+    res = run_ours(args, dist)
+    if dist.rank == 0:
+        print(json.dumps(res), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,152 @@
+// EAGLE3 small-vocabulary mapping: scatter draft logits into the target
+// vocabulary and build the inverse map.
+//
+// Source: "SSD: extending the engine with new models and an EAGLE3 draft"
+// §六: the draft lm_head covers only draft_vocab_size ids; d2t/t2d map the
+// small-vocabulary logits back into the full target vocabulary.
+#include "sv_internal.h"
+
+#include <cstring>
+
+namespace sv {
+
+// Gather form: every output element is written exactly once,
+// out[r, t] = t2d[t] >= 0 ? in[r, t2d[t]] : fill.  One thread per 16-byte
+// output vector; t2d is read as int4.
+template <typename E, int THREADS>
+__global__ void __launch_bounds__(THREADS)
+scatter_gather_kernel(const E* __restrict__ in, int64_t in_stride, const int32_t* __restrict__ t2d,
+                      int vd, int V, E fill, E* __restrict__ out, int64_t out_stride, int tiles) {
+  constexpr int EPV = Elem<E>::kPerVec;
+  const int row = blockIdx.x / tiles;
+  const int tile = blockIdx.x - row * tiles;
+  const E* src = in + static_cast<int64_t>(row) * in_stride;
+  E* dst = out + static_cast<int64_t>(row) * out_stride;
+  const int v = tile * THREADS + threadIdx.x;
+  const int t0 = v * EPV;
+  if (t0 + EPV <= V) {
+    int32_t ids[EPV];
+#pragma unroll
+    for (int q = 0; q < EPV / 4; ++q) {
+      const int4 w = __ldg(reinterpret_cast<const int4*>(t2d + t0) + q);
+      ids[4 * q + 0] = w.x;
+      ids[4 * q + 1] = w.y;
+      ids[4 * q + 2] = w.z;
+      ids[4 * q + 3] = w.w;
+    }
+    E vals[EPV];
+#pragma unroll
+    for (int e = 0; e < EPV; ++e) {
+      const int j = ids[e];
+      vals[e] = (j >= 0 && j < vd) ? src[j] : fill;
+    }
+    *reinterpret_cast<uint4*>(dst + t0) = *reinterpret_cast<const uint4*>(vals);
+  } else if (t0 < V) {
+    for (int t = t0; t < V; ++t) {
+      const int j = t2d[t];
+      dst[t] = (j >= 0 && j < vd) ? src[j] : fill;
+    }
+  }
+}
+
+// Scatter form (no t2d): one block per row fills the row, then writes the
+// draft values at their target ids.  The barrier orders the two phases.
+template <typename E, int THREADS>
+__global__ void __launch_bounds__(THREADS)
+scatter_fill_kernel(const E* __restrict__ in, int64_t in_stride, const int32_t* __restrict__ d2t,
+                    int vd, int V, E fill, E* __restrict__ out, int64_t out_stride) {
+  constexpr int EPV = Elem<E>::kPerVec;
+  const int row = blockIdx.x;
+  const E* src = in + static_cast<int64_t>(row) * in_stride;
+  E* dst = out + static_cast<int64_t>(row) * out_stride;
+  E fv[EPV];
+#pragma unroll
+  for (int e = 0; e < EPV; ++e) fv[e] = fill;
+  const uint4 fvec = *reinterpret_cast<const uint4*>(fv);
+  const int nvec = V / EPV;
+  for (int v = threadIdx.x; v < nvec; v += THREADS) reinterpret_cast<uint4*>(dst)[v] = fvec;
+  for (int t = nvec * EPV + threadIdx.x; t < V; t += THREADS) dst[t] = fill;
+  __syncthreads();
+  for (int j = threadIdx.x; j < vd; j += THREADS) {
+    const int x = __ldg(d2t + j);
+    if (x >= 0 && x < V) dst[x] = src[j];
+  }
+}
+
+__global__ void t2d_fill_kernel(int32_t* t2d, int V, int32_t* status) {
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  if (t < V) t2d[t] = -1;
+  if (t == 0 && status) *status = 0;
+}
+
+__global__ void t2d_set_kernel(const int32_t* d2t, int vd, int V, int32_t* t2d, int32_t* status) {
+  const int j = blockIdx.x * blockDim.x + threadIdx.x;
+  if (j >= vd) return;
+  const int x = d2t[j];
+  if (x < 0 || x >= V) {
+    if (status) atomicOr(status, 1);
+    return;
+  }
+  const int old = atomicCAS(t2d + x, -1, j);
+  if (old != -1 && status) atomicOr(status, 2);
+}
+
+template <typename E>
+static E to_elem(float f);
+template <>
+float to_elem<float>(float f) {
+  return f;
+}
+template <>
+uint16_t to_elem<uint16_t>(float f) {
+  // Round to nearest even; infinities and NaN keep their class.
+  uint32_t u;
+  std::memcpy(&u, &f, 4);
+  if ((u & 0x7f800000u) == 0x7f800000u) return static_cast<uint16_t>((u >> 16) | ((u & 0xffffu) ? 0x40u : 0u));
+  u += 0x7fffu + ((u >> 16) & 1u);
+  return static_cast<uint16_t>(u >> 16);
+}
+
+template <typename E>
+static sv_status scatter_impl(const void* in, int64_t in_stride, const int32_t* d2t,
+                              const int32_t* t2d, int rows, int vd, int V, float fill, void* out,
+                              int64_t out_stride, cudaStream_t stream) {
+  constexpr int kThreads = 256;
+  if (rows == 0) return SV_OK;
+  const E f = to_elem<E>(fill);
+  if (t2d) {
+    const int nv = (V + Elem<E>::kPerVec - 1) / Elem<E>::kPerVec;
+    const int tiles = (nv + kThreads - 1) / kThreads;
+    scatter_gather_kernel<E, kThreads><<<static_cast<unsigned>(rows) * tiles, kThreads, 0, stream>>>(
+        static_cast<const E*>(in), in_stride, t2d, vd, V, f, static_cast<E*>(out), out_stride, tiles);
+  } else {
+    scatter_fill_kernel<E, 1024><<<rows, 1024, 0, stream>>>(static_cast<const E*>(in), in_stride, d2t,
+                                                            vd, V, f, static_cast<E*>(out), out_stride);
+  }
+  if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
+  note_launch(stream);
+  return SV_OK;
+}
+
+sv_status d2t_scatter(const void* in, int64_t in_stride, const int32_t* d2t, const int32_t* t2d,
+                      int rows, int vd, int v, sv_dtype dtype, float fill, void* out,
+                      int64_t out_stride, cudaStream_t stream) {
+  return dtype == SV_BF16
+             ? scatter_impl<uint16_t>(in, in_stride, d2t, t2d, rows, vd, v, fill, out, out_stride, stream)
+             : scatter_impl<float>(in, in_stride, d2t, t2d, rows, vd, v, fill, out, out_stride, stream);
+}
+
+sv_status build_t2d(const int32_t* d2t, int vd, int v, int32_t* t2d, int32_t* status,
+                    cudaStream_t stream) {
+  t2d_fill_kernel<<<(v + 255) / 256, 256, 0, stream>>>(t2d, v, status);
+  if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
+  note_launch(stream);
+  if (vd > 0) {
+    t2d_set_kernel<<<(vd + 255) / 256, 256, 0, stream>>>(d2t, vd, v, t2d, status);
+    if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
+    note_launch(stream);
+  }
+  return SV_OK;
+}
+
+}  // namespace sv

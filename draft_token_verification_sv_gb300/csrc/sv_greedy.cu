@@ -1,0 +1,327 @@
+// Greedy (temperature 0) verify: argmax of every target row, then the
+// per-group decision (chain prefix match or tree walk) by the last block of
+// the group to finish, all in one launch.
+//
+// Sources: "SSD: extending the engine with new models and an EAGLE3 draft"
+// §七 (--temp 0 benchmarking); "A 2.16x speculative-decoding speedup from a
+// 1-layer Llama draft", headline table ("Match = True": greedy speculative
+// output equals greedy decoding) and §5 (draft token tree).
+#include "sv_internal.h"
+
+namespace sv {
+
+enum class GreedyMode : int { kChain = 0, kTree = 1, kSample = 2 };
+
+struct GreedyParams {
+  const void* logits;
+  int64_t stride;
+  int V;
+  int rows_per_group;  // γ+1 (chain), N (tree), 1 (sample)
+  int groups;
+  int32_t* g;          // [rows] argmax per row, -1 for a row with no finite logit
+  unsigned int* counters;  // [groups], zero between calls
+  // chain
+  const int32_t* draft_ids;
+  int32_t* out_tokens;
+  int32_t* num_accepted;
+  float* p_draft;
+  float* q_draft;
+  int32_t* row_status;
+  // tree
+  const int32_t* parents;
+  const int32_t* tokens;
+  int32_t* accept_len;
+  int32_t* path;
+  int max_depth;
+  // sample
+  float* out_prob;
+};
+
+// Largest value with the lowest index over one row, packed (see argmax_pack);
+// the result is valid in every thread.
+template <typename E, int THREADS, int UNROLL>
+__device__ __forceinline__ unsigned long long row_argmax(const E* row, int V,
+                                                         unsigned long long* scratch) {
+  constexpr int EPV = Elem<E>::kPerVec;
+  const int nvec = V / EPV;
+  const uint4* vp = reinterpret_cast<const uint4*>(row);
+  float bv = -CUDART_INF_F;
+  int bi = 0x7fffffff;
+  for (int v0 = threadIdx.x; v0 < nvec; v0 += THREADS * UNROLL) {
+    uint4 buf[UNROLL];
+#pragma unroll
+    for (int u = 0; u < UNROLL; ++u) {
+      const int v = v0 + u * THREADS;
+      buf[u] = v < nvec ? ldg_stream(vp + v) : Elem<E>::neg_inf_vec();
+    }
+#pragma unroll
+    for (int u = 0; u < UNROLL; ++u) {
+      float x[EPV];
+      unpack<E>(buf[u], x);
+      float vm = x[0];
+#pragma unroll
+      for (int i = 1; i < EPV; ++i) vm = fmaxf(vm, x[i]);
+      if (vm > bv) {
+        int first = EPV - 1;
+#pragma unroll
+        for (int i = EPV - 1; i >= 0; --i)
+          if (x[i] == vm) first = i;
+        bv = vm;
+        bi = (v0 + u * THREADS) * EPV + first;
+      }
+    }
+  }
+  const int tail = nvec * EPV + static_cast<int>(threadIdx.x);
+  if (tail < V) {
+    const float x = Elem<E>::load(row + tail);
+    if (x > bv) {
+      bv = x;
+      bi = tail;
+    }
+  }
+  // A thread that saw only -inf proposes index 0 (np.argmax convention).
+  const unsigned long long packed = bi == 0x7fffffff ? argmax_pack(-CUDART_INF_F, 0)
+                                                     : argmax_pack(bv, bi);
+  return block_max_u64<THREADS>(packed, scratch);
+}
+
+template <int THREADS>
+__device__ void chain_decide(const GreedyParams& P, int b) {
+  // Single thread: γ <= 64 comparisons.
+  if (threadIdx.x != 0) return;
+  const int G = P.rows_per_group - 1;
+  const int32_t* g = P.g + static_cast<int64_t>(b) * (G + 1);
+  const int32_t* ids = P.draft_ids + static_cast<int64_t>(b) * G;
+  int32_t* out = P.out_tokens + static_cast<int64_t>(b) * (G + 1);
+  uint32_t status = 0;
+  for (int i = 0; i < G; ++i) {
+    const int x = ids[i];
+    if (x < 0 || x >= P.V) status |= SV_ROW_BAD_DRAFT_ID;
+  }
+  for (int i = 0; i <= G; ++i)
+    if (__ldcg(g + i) < 0) status |= SV_ROW_EMPTY;
+  int k = 0;
+  if (!status) {
+    k = G;
+    for (int i = 0; i < G; ++i) {
+      if (ids[i] != __ldcg(g + i)) {
+        k = i;
+        break;
+      }
+    }
+    for (int i = 0; i < k; ++i) out[i] = ids[i];
+    out[k] = __ldcg(g + k);
+    for (int i = k + 1; i <= G; ++i) out[i] = -1;
+  } else {
+    for (int i = 0; i <= G; ++i) out[i] = -1;
+  }
+  P.num_accepted[b] = k;
+  if (P.row_status) P.row_status[b] = static_cast<int32_t>(status);
+  if (P.p_draft)
+    for (int i = 0; i < G; ++i) P.p_draft[static_cast<int64_t>(b) * G + i] = 0.0f;
+  if (P.q_draft)
+    for (int i = 0; i < G; ++i) P.q_draft[static_cast<int64_t>(b) * G + i] = 0.0f;
+}
+
+template <int THREADS>
+__device__ void tree_walk(const GreedyParams& P, int b) {
+  // Nodes are handled in a block-strided loop (N <= SV_MAX_TREE_NODES).
+  __shared__ int s_par[SV_MAX_TREE_NODES];
+  __shared__ int s_tok[SV_MAX_TREE_NODES];
+  __shared__ int s_g[SV_MAX_TREE_NODES];
+  __shared__ int s_depth[SV_MAX_TREE_NODES];
+  __shared__ unsigned char s_acc[SV_MAX_TREE_NODES];
+  __shared__ unsigned int s_status;
+  __shared__ unsigned long long s_red[32];
+  const int N = P.rows_per_group;
+  const int D = P.max_depth;
+  const int64_t base = static_cast<int64_t>(b) * N;
+  if (threadIdx.x == 0) s_status = 0;
+  __syncthreads();
+  for (int n = threadIdx.x; n < N; n += THREADS) {
+    const int par = P.parents[base + n];
+    const int tok = P.tokens[base + n];
+    const int gv = __ldcg(P.g + base + n);
+    s_par[n] = par;
+    s_tok[n] = tok;
+    s_g[n] = gv;
+    s_acc[n] = n == 0 ? 1 : 0;
+    s_depth[n] = 0;
+    uint32_t st = 0;
+    if (n == 0 ? par != -1 : (par < 0 || par >= n)) st |= SV_ROW_BAD_PARENT;
+    if (n > 0 && (tok < 0 || tok >= P.V)) st |= SV_ROW_BAD_TOKEN;
+    if (gv < 0) st |= SV_ROW_EMPTY;
+    if (st) atomicOr(&s_status, st);
+  }
+  __syncthreads();
+  if (!(s_status & SV_ROW_BAD_PARENT)) {
+    for (int n = threadIdx.x; n < N; n += THREADS) {
+      // parents[m] < m: the walk reaches the root; D+1 steps are enough to
+      // tell that a node is deeper than D.
+      int d = 0, cur = n;
+      for (int step = 0; step <= D && cur > 0; ++step) {
+        cur = s_par[cur];
+        ++d;
+      }
+      if (cur > 0) atomicOr(&s_status, SV_ROW_DEPTH_EXCEEDED);
+      s_depth[n] = d;
+    }
+  }
+  __syncthreads();
+  const uint32_t status = s_status;
+  int32_t* out = P.out_tokens + static_cast<int64_t>(b) * (D + 1);
+  int32_t* path = P.path + static_cast<int64_t>(b) * (D + 1);
+  if (status) {
+    for (int d = threadIdx.x; d <= D; d += THREADS) {
+      out[d] = -1;
+      path[d] = -1;
+    }
+    if (threadIdx.x == 0) {
+      P.accept_len[b] = 0;
+      if (P.row_status) P.row_status[b] = static_cast<int32_t>(status);
+    }
+    return;
+  }
+  // Level by level: a node is accepted iff its parent is and its token is
+  // the argmax of the parent's row.
+  for (int lvl = 1; lvl <= D; ++lvl) {
+    __syncthreads();
+    for (int n = threadIdx.x; n < N; n += THREADS)
+      if (s_depth[n] == lvl) {
+        const int par = s_par[n];
+        s_acc[n] = (s_acc[par] && s_tok[n] == s_g[par]) ? 1 : 0;
+      }
+  }
+  __syncthreads();
+  unsigned long long key = 0;
+  for (int n = threadIdx.x; n < N; n += THREADS)
+    if (s_acc[n]) {
+      const unsigned long long k =
+          (static_cast<unsigned long long>(s_depth[n]) << 32) | (0xffffffffu - static_cast<uint32_t>(n));
+      key = k > key ? k : key;
+    }
+  key = block_max_u64<THREADS>(key, s_red);
+  const int best = static_cast<int>(0xffffffffu - static_cast<uint32_t>(key & 0xffffffffull));
+  const int L = static_cast<int>(key >> 32);
+  if (threadIdx.x == 0) {
+    int cur = best;
+    for (int d = L; d >= 0; --d) {  // L <= D steps
+      path[d] = cur;
+      if (d > 0) out[d - 1] = s_tok[cur];
+      if (d > 0) cur = s_par[cur];
+    }
+    out[L] = s_g[best];
+    for (int d = L + 1; d <= D; ++d) {
+      path[d] = -1;
+      out[d] = -1;
+    }
+    P.accept_len[b] = L;
+    if (P.row_status) P.row_status[b] = 0;
+  }
+}
+
+template <typename E, int THREADS, int UNROLL, GreedyMode MODE>
+__global__ void __launch_bounds__(THREADS) greedy_kernel(GreedyParams P) {
+  __shared__ unsigned long long s_red[32];
+  __shared__ bool s_last;
+  const int row = blockIdx.x;
+  const E* rp = reinterpret_cast<const E*>(P.logits) + static_cast<int64_t>(row) * P.stride;
+  const unsigned long long best = row_argmax<E, THREADS, UNROLL>(rp, P.V, s_red);
+  const bool empty = (best >> 32) == static_cast<unsigned long long>(order_key(-CUDART_INF_F));
+  const int idx = empty ? -1 : argmax_index(best);
+  if constexpr (MODE == GreedyMode::kSample) {
+    if (threadIdx.x == 0) {
+      P.out_tokens[row] = empty ? -1 : idx;
+      if (P.out_prob) P.out_prob[row] = empty ? 0.0f : 1.0f;
+    }
+    return;
+  } else {
+    const int group = row / P.rows_per_group;
+    if (threadIdx.x == 0) {
+      P.g[row] = idx;
+      __threadfence();
+      const unsigned int prev = atomicAdd(P.counters + group, 1u);
+      s_last = prev == static_cast<unsigned int>(P.rows_per_group - 1);
+      if (s_last) P.counters[group] = 0u;  // leave the workspace zeroed
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    if constexpr (MODE == GreedyMode::kChain) chain_decide<THREADS>(P, group);
+    else tree_walk<THREADS>(P, group);
+  }
+}
+
+template <typename E, GreedyMode MODE>
+static sv_status launch_greedy(const GreedyParams& P, int rows, cudaStream_t stream) {
+  constexpr int kThreads = 512;
+  constexpr int kUnroll = 4;
+  if (rows == 0) return SV_OK;
+  greedy_kernel<E, kThreads, kUnroll, MODE><<<rows, kThreads, 0, stream>>>(P);
+  if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
+  note_launch(stream);
+  return SV_OK;
+}
+
+sv_status greedy_chain(const sv_chain_desc& d, const void* target, const int32_t* ids,
+                       int32_t* out_tokens, int32_t* num_accepted, float* p_draft, float* q_draft,
+                       int32_t* row_status, void* workspace, cudaStream_t stream) {
+  const int rows = d.batch * (d.gamma + 1);
+  GreedyParams P{};
+  P.logits = target;
+  P.stride = d.target_row_stride;
+  P.V = d.vocab;
+  P.rows_per_group = d.gamma + 1;
+  P.groups = d.batch;
+  WorkspaceLayout L = chain_workspace_layout(d);
+  P.counters = reinterpret_cast<unsigned int*>(static_cast<char*>(workspace) + L.counters);
+  P.g = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + L.argmax);
+  P.draft_ids = ids;
+  P.out_tokens = out_tokens;
+  P.num_accepted = num_accepted;
+  P.p_draft = p_draft;
+  P.q_draft = q_draft;
+  P.row_status = row_status;
+  return d.target_dtype == SV_BF16 ? launch_greedy<uint16_t, GreedyMode::kChain>(P, rows, stream)
+                                   : launch_greedy<float, GreedyMode::kChain>(P, rows, stream);
+}
+
+sv_status greedy_tree(const sv_tree_desc& d, const void* logits, const int32_t* parents,
+                      const int32_t* tokens, int32_t* accept_len, int32_t* path,
+                      int32_t* out_tokens, int32_t* row_status, void* workspace,
+                      cudaStream_t stream) {
+  GreedyParams P{};
+  P.logits = logits;
+  P.stride = d.row_stride;
+  P.V = d.vocab;
+  P.rows_per_group = d.nodes;
+  P.groups = d.batch;
+  P.counters = static_cast<unsigned int*>(workspace);
+  P.g = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + tree_counter_bytes(d.batch));
+  P.parents = parents;
+  P.tokens = tokens;
+  P.accept_len = accept_len;
+  P.path = path;
+  P.out_tokens = out_tokens;
+  P.row_status = row_status;
+  P.max_depth = d.max_depth;
+  const int rows = d.batch * d.nodes;
+  return d.dtype == SV_BF16 ? launch_greedy<uint16_t, GreedyMode::kTree>(P, rows, stream)
+                            : launch_greedy<float, GreedyMode::kTree>(P, rows, stream);
+}
+
+sv_status greedy_sample(const sv_sample_desc& d, const void* logits, int32_t* out_tokens,
+                        float* out_prob, cudaStream_t stream) {
+  GreedyParams P{};
+  P.logits = logits;
+  P.stride = d.row_stride;
+  P.V = d.vocab;
+  P.rows_per_group = 1;
+  P.groups = d.rows;
+  P.out_tokens = out_tokens;
+  P.out_prob = out_prob;
+  return d.dtype == SV_BF16 ? launch_greedy<uint16_t, GreedyMode::kSample>(P, d.rows, stream)
+                            : launch_greedy<float, GreedyMode::kSample>(P, d.rows, stream);
+}
+
+}  // namespace sv

@@ -1,0 +1,86 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include "sv_common.cuh"
+
+#include <atomic>
+
+namespace sv {
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Call after every kernel launch: counts launches and records the caller's
+// phase event for this launch, if one is pending (see sv_set_phase_events).
+void note_launch(cudaStream_t stream);
+// Drop any phase events left over when a call returns.
+void end_call();
+
+// Per-kernel cache of the attributes set with cudaFuncSetAttribute, per
+// device, so a call only touches them when it needs more than any earlier
+// call did (repeated calls, and calls under stream capture, make none).
+struct FuncAttrCache {
+  static constexpr int kMaxDevices = 64;
+  std::atomic<size_t> smem[kMaxDevices] = {};
+  std::atomic<int> nonportable[kMaxDevices] = {};
+  bool ensure(const void* func, size_t dyn_smem, bool non_portable_cluster);
+};
+
+// Chain workspace: [counters: B u32][stats: B(2γ+1) RowStats][argmax: B(γ+1) i32]
+struct WorkspaceLayout {
+  size_t counters, stats, argmax, total;
+};
+
+inline WorkspaceLayout chain_workspace_layout(const sv_chain_desc& d) {
+  WorkspaceLayout L{};
+  const size_t B = static_cast<size_t>(d.batch);
+  const size_t G = static_cast<size_t>(d.gamma);
+  L.counters = 0;
+  L.stats = align_up(B * sizeof(uint32_t), 256);
+  L.argmax = L.stats + align_up(B * (2 * G + 1) * sizeof(RowStats), 256);
+  L.total = L.argmax + align_up(B * (G + 1) * sizeof(int32_t), 256);
+  return L;
+}
+
+inline size_t tree_counter_bytes(int batch) {
+  return align_up(static_cast<size_t>(batch) * sizeof(uint32_t), 256);
+}
+
+// Entry points of the individual paths (arguments already validated).
+sv_status greedy_chain(const sv_chain_desc& d, const void* target, const int32_t* ids,
+                       int32_t* out_tokens, int32_t* num_accepted, float* p_draft, float* q_draft,
+                       int32_t* row_status, void* workspace, cudaStream_t stream);
+sv_status greedy_tree(const sv_tree_desc& d, const void* logits, const int32_t* parents,
+                      const int32_t* tokens, int32_t* accept_len, int32_t* path,
+                      int32_t* out_tokens, int32_t* row_status, void* workspace,
+                      cudaStream_t stream);
+sv_status greedy_sample(const sv_sample_desc& d, const void* logits, int32_t* out_tokens,
+                        float* out_prob, cudaStream_t stream);
+
+struct ChainArgs {
+  sv_chain_desc d;
+  const void* target;
+  const void* draft;
+  const int32_t* d2t;
+  const int32_t* t2d;
+  const int32_t* ids;
+  const float* u_accept;
+  const float* u_resample;
+  int32_t* out_tokens;
+  int32_t* num_accepted;
+  float* p_draft;
+  float* q_draft;
+  int32_t* row_status;
+  void* workspace;
+};
+sv_status sampling_chain(const ChainArgs& a, cudaStream_t stream);
+
+sv_status sample_rows(const sv_sample_desc& d, const void* logits, const float* u,
+                      int32_t* out_tokens, float* out_prob, void* workspace, cudaStream_t stream);
+
+sv_status d2t_scatter(const void* in, int64_t in_stride, const int32_t* d2t, const int32_t* t2d,
+                      int rows, int vd, int v, sv_dtype dtype, float fill, void* out,
+                      int64_t out_stride, cudaStream_t stream);
+sv_status build_t2d(const int32_t* d2t, int vd, int v, int32_t* t2d, int32_t* status,
+                    cudaStream_t stream);
+
+}  // namespace sv

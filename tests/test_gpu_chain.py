@@ -1,0 +1,230 @@
+"""Chain verify on the GPU (through the C-ABI) against the fp64 oracle.
+
+Workloads are the pages' settings restated (tiny, SmolLM2-shaped, Llama-3
+vocabulary greedy and sampling, Qwen3 vocabulary with an EAGLE3 draft
+vocabulary) plus small randomised shapes with ties, padding, degenerate
+sizes and malformed ids."""
+import math
+
+import numpy as np
+import pytest
+
+import synth
+from oracle import sv_oracle as O
+
+from _parity import (chain_properties, compare_chain, logits_tensor, oracle_chain, oracle_draft_ids,
+                     run_chain, t)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def sv():
+    import __graft_entry__
+    __graft_entry__.build()
+    import draft_token_verification_sv_gb300 as sv
+    return sv
+
+
+def _report(name, res):
+    n, near, near_mis, rel = res
+    print(f"[{name}] rows={n} near-threshold={near} near-threshold mismatches={near_mis} "
+          f"max rel prob err={rel:.2e}")
+
+
+def test_tiny_many_rows(sv):
+    """The tiny workload's shape (γ=3, V=1000 fp32, T=0.8, top_p=0.9) over 400 seeded rows."""
+    x = synth.make_chain_inputs(synth.TINY, batch=400)
+    ids = oracle_draft_ids(x)
+    got = run_chain(sv, x, ids)
+    want = oracle_chain(x, ids)
+    res = compare_chain(got, want, ids, "f32")
+    _report("tiny x400", res)
+    ks = got["num_accepted"]
+    assert (ks == 0).any() and (ks == 3).any()   # both branches exercised
+
+
+def test_smollm2_full(sv):
+    x = synth.make_chain_inputs(synth.SMOLLM2)
+    ids = oracle_draft_ids(x)
+    got = run_chain(sv, x, ids)
+    want = oracle_chain(x, ids)
+    _report("smollm2", compare_chain(got, want, ids, "bf16"))
+
+
+def test_llama3_sampling_full(sv):
+    x = synth.make_chain_inputs(synth.LLAMA3_SAMPLE)
+    ids = oracle_draft_ids(x)
+    got = run_chain(sv, x, ids)
+    want = oracle_chain(x, ids)
+    _report("llama3 T=1", compare_chain(got, want, ids, "bf16"))
+
+
+def test_llama3_greedy_full(sv):
+    x = synth.make_chain_inputs(synth.LLAMA3_GREEDY)
+    ids = oracle_draft_ids(x)
+    got = run_chain(sv, x, ids)
+    want = oracle_chain(x, ids)
+    assert np.array_equal(got["tokens"], want["tokens"])
+    assert np.array_equal(got["num_accepted"], want["num_accepted"])
+    assert np.all(got["row_status"] == 0)
+
+
+@pytest.fixture(scope="module")
+def qwen3(sv):
+    x = synth.make_chain_inputs(synth.QWEN3_D2T)
+    ids = oracle_draft_ids(x)
+    return x, ids
+
+
+def test_qwen3_d2t_full_size(sv, qwen3):
+    """Full Qwen3/EAGLE3 workload: every row checked for validity, a seeded
+    sample of rows checked against the oracle."""
+    x, ids = qwen3
+    got = run_chain(sv, x, ids)
+    chain_properties(got, ids, x["vocab"])
+    rows = sorted(np.random.default_rng(7).choice(x["batch"], 12, replace=False).tolist())
+    want = oracle_chain(x, ids, rows=rows)
+    _report("qwen3 d2t (sampled rows)", compare_chain(got, want, ids, "f32", rows=rows))
+
+
+def test_qwen3_d2t_repeat_is_identical(sv, qwen3):
+    """Two calls in a row give the same bits (deterministic, workspace reset)."""
+    x, ids = qwen3
+    a = run_chain(sv, x, ids)
+    b = run_chain(sv, x, ids)
+    for k in a:
+        assert np.array_equal(a[k], b[k]), k
+
+
+def _case(V, G, dtype, T, top_p, ties, B=6, seed=0, shuffled=False, d2t_frac=0.0):
+    cfg = synth.ChainConfig("case", B, G, V, dtype, T, top_p, 2.0, 0.6,
+                            draft_vocab=max(1, int(V * d2t_frac)) if d2t_frac else 0)
+    x = synth.make_chain_inputs(cfg, seed=seed, shuffled_d2t=shuffled)
+    if ties:
+        # Quantise so that many logits are exactly equal (ties in argmax and top-p).
+        for key in ("target", "draft"):
+            q = (np.round(x[key] * 2.0) / 2.0).astype(np.float32)
+            x[key] = q
+            x[key + "_store"] = synth.to_bf16_bits(q) if dtype == "bf16" else q
+    return x
+
+
+SMALL = [(V, G) for V in (1, 2, 3, 7, 31, 1000, 4097) for G in (0, 1, 3, 8)]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("V,G", SMALL)
+def test_small_shapes_sampling(sv, V, G, dtype):
+    for seed, (T, top_p, ties) in enumerate([(1.0, 1.0, False), (0.7, 0.8, True), (1.3, 0.5, False)]):
+        x = _case(V, G, dtype, T, top_p, ties, seed=100 * V + 10 * G + seed)
+        ids = oracle_draft_ids(x)
+        got = run_chain(sv, x, ids)
+        want = oracle_chain(x, ids)
+        compare_chain(got, want, ids, dtype)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("V,G", [(1, 2), (7, 3), (31, 8), (4097, 5)])
+def test_small_shapes_greedy(sv, V, G, dtype):
+    x = _case(V, G, dtype, 0.0, 1.0, ties=True, B=16, seed=V + G)
+    ids = oracle_draft_ids(x)
+    # Force some drafts to mismatch, some to match.
+    ids[::2, -1:] = (ids[::2, -1:] + 1) % V
+    got = run_chain(sv, x, ids)
+    want = oracle_chain(x, ids)
+    assert np.array_equal(got["tokens"], want["tokens"])
+    assert np.array_equal(got["num_accepted"], want["num_accepted"])
+
+
+@pytest.mark.parametrize("shuffled", [False, True])
+@pytest.mark.parametrize("ties", [False, True])
+def test_d2t_small(sv, shuffled, ties):
+    x = _case(20000, 4, "f32", 0.9, 0.9, ties, B=8, seed=3, shuffled=shuffled, d2t_frac=0.2)
+    ids = oracle_draft_ids(x)
+    got = run_chain(sv, x, ids)
+    want = oracle_chain(x, ids)
+    compare_chain(got, want, ids, "f32")
+
+
+def test_q_equals_p_accepts_everything(sv):
+    x = _case(5000, 6, "bf16", 0.8, 0.9, ties=False, B=32, seed=11)
+    x["draft"] = x["target"][:, :6].copy()
+    x["draft_store"] = x["target_store"][:, :6].copy()
+    ids = oracle_draft_ids(x)
+    got = run_chain(sv, x, ids)
+    assert np.all(got["num_accepted"] == 6)
+    want = oracle_chain(x, ids)
+    compare_chain(got, want, ids, "bf16")
+
+
+def test_padded_rows(sv):
+    """Rows that live in a wider buffer (row stride > V)."""
+    import torch
+    x = _case(1003, 3, "f32", 1.0, 0.95, ties=False, B=5, seed=5)
+    ids = oracle_draft_ids(x)
+    pad = 1008
+    tgt = torch.full((5, 4, pad), 7.0, device="cuda")
+    drf = torch.full((5, 3, pad), 7.0, device="cuda")
+    tgt[..., :1003] = t(x["target"])
+    drf[..., :1003] = t(x["draft"])
+    got = sv.verify_chain(tgt[..., :1003], drf[..., :1003], t(ids), t(x["u_accept"]), t(x["u_resample"]),
+                          1.0, 0.95)
+    torch.cuda.synchronize()
+    got = {k: v.cpu().numpy() for k, v in got.items()}
+    compare_chain(got, oracle_chain(x, ids), ids, "f32")
+
+
+def test_mixed_dtypes(sv):
+    """bf16 target rows with fp32 draft rows."""
+    import torch
+    x = _case(3000, 4, "bf16", 1.0, 0.9, ties=False, B=8, seed=9)
+    x["draft_store"] = x["draft"].astype(np.float32)  # exact values of the bf16 draft
+    ids = oracle_draft_ids(x)
+    got = sv.verify_chain(logits_tensor(x["target_store"], "bf16"), logits_tensor(x["draft_store"], "f32"),
+                          t(ids), t(x["u_accept"]), t(x["u_resample"]), 1.0, 0.9)
+    torch.cuda.synchronize()
+    got = {k: v.cpu().numpy() for k, v in got.items()}
+    compare_chain(got, oracle_chain(x, ids), ids, "bf16")
+
+
+def test_bad_ids_and_empty_rows(sv):
+    x = _case(300, 3, "f32", 1.0, 0.9, ties=False, B=6, seed=21)
+    ids = oracle_draft_ids(x)
+    ids[1, 2] = 300          # out of range
+    ids[2, 0] = -5
+    x["target"][3, 1, :] = -np.inf   # a target row with no finite logit
+    x["target_store"] = x["target"]
+    x["draft"][4, 2, :] = -np.inf
+    x["draft_store"] = x["draft"]
+    got = run_chain(sv, x, ids)
+    want = oracle_chain(x, ids)
+    for b in (1, 2):
+        assert got["row_status"][b] & O.STATUS_BAD_DRAFT_ID
+        assert got["num_accepted"][b] == 0 and np.all(got["tokens"][b] == -1)
+    for b in (3, 4):
+        assert got["row_status"][b] & O.STATUS_EMPTY_ROW
+        assert np.all(got["tokens"][b] == -1)
+    compare_chain(got, want, ids, "f32", rows=[0, 5])
+    # Greedy path flags the same ids.
+    g = run_chain(sv, x, ids, temperature=0.0, top_p=1.0)
+    assert g["row_status"][1] & O.STATUS_BAD_DRAFT_ID and g["row_status"][3] & O.STATUS_EMPTY_ROW
+
+
+def test_neg_inf_entries(sv):
+    x = _case(2000, 3, "bf16", 1.0, 0.9, ties=False, B=8, seed=4)
+    rng = np.random.default_rng(0)
+    mask = rng.random(x["target"].shape) < 0.3
+    x["target"][mask] = -np.inf
+    x["target_store"] = synth.to_bf16_bits(x["target"])
+    ids = oracle_draft_ids(x)
+    compare_chain(run_chain(sv, x, ids), oracle_chain(x, ids), ids, "bf16")
+
+
+def test_empty_batch(sv):
+    import torch
+    tgt = torch.zeros((0, 4, 64), device="cuda")
+    out = sv.verify_chain(tgt, torch.zeros((0, 3, 64), device="cuda"),
+                          torch.zeros((0, 3), dtype=torch.int32, device="cuda"),
+                          torch.zeros((0, 3), device="cuda"), torch.zeros(0, device="cuda"), 1.0, 0.9)
+    assert out["tokens"].shape == (0, 4)

@@ -1,0 +1,156 @@
+"""Tree verify, d2t scatter, t2d build and draft-side sampling on the GPU
+(through the C-ABI) against the fp64 oracle."""
+import math
+
+import numpy as np
+import pytest
+
+import synth
+from oracle import sv_oracle as O
+
+from _parity import logits_tensor, t
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def sv():
+    import __graft_entry__
+    __graft_entry__.build()
+    import draft_token_verification_sv_gb300 as sv
+    return sv
+
+
+def _tree_run(sv, tr, dtype="bf16"):
+    import torch
+    logits = logits_tensor(tr["logits_store"], dtype)
+    got = sv.verify_tree(logits, t(tr["parents"]), t(tr["tokens"]), tr["max_depth"])
+    torch.cuda.synchronize()
+    return {k: v.cpu().numpy() for k, v in got.items()}
+
+
+def _tree_compare(got, want):
+    assert np.array_equal(got["accept_len"], want["accept_len"])
+    assert np.array_equal(got["out_tokens"], want["out_tokens"])
+    assert np.array_equal(got["path"], want["path"])
+    assert np.array_equal(got["row_status"] != 0, want["status"] != 0)
+
+
+def test_tree_full_workload(sv):
+    """64 trees x 32 nodes, V = 128256 bf16 (the Eaglet1 tree budget)."""
+    tr = synth.make_tree_inputs(synth.TREE)
+    got = _tree_run(sv, tr)
+    want = O.verify_tree(tr["logits"], tr["parents"], tr["tokens"], tr["max_depth"])
+    _tree_compare(got, want)
+    print(f"[tree] mean accepted length {got['accept_len'].mean():.2f}")
+    assert got["accept_len"].max() >= 2
+
+
+@pytest.mark.parametrize("N,V,D,dtype", [(1, 5, 0, "bf16"), (2, 3, 1, "f32"), (12, 4, 4, "bf16"),
+                                         (32, 7, 5, "f32"), (600, 3, 64, "bf16"), (1024, 2, 12, "f32")])
+def test_tree_small_with_ties(sv, N, V, D, dtype):
+    cfg = synth.TreeConfig("t", 5, N, V, dtype, D, 8 if N <= 32 else 64, 1.0, 0.8, 0.0)
+    tr = synth.make_tree_inputs(cfg, seed=N * 7 + V)
+    q = np.round(tr["logits"]).astype(np.float32)   # ties everywhere
+    tr["logits"] = q
+    tr["logits_store"] = synth.to_bf16_bits(q) if dtype == "bf16" else q
+    # Plant matches so paths are long: child token = parent's argmax.
+    for b in range(tr["batch"]):
+        for n in range(1, N):
+            if n % 3:
+                tr["tokens"][b, n] = int(np.argmax(q[b, tr["parents"][b, n]]))
+    got = _tree_run(sv, tr, dtype)
+    want = O.verify_tree(tr["logits"], tr["parents"], tr["tokens"], tr["max_depth"])
+    _tree_compare(got, want)
+
+
+def test_tree_invalid(sv):
+    tr = synth.make_tree_inputs(synth.TREE, batch=4, vocab=257)
+    tr["parents"][1, 5] = 9          # parent after child
+    tr["parents"][2, 0] = 0          # root with a parent
+    tr["tokens"][3, 4] = 257         # token out of range
+    got = _tree_run(sv, tr)
+    want = O.verify_tree(tr["logits"], tr["parents"], tr["tokens"], tr["max_depth"])
+    assert got["row_status"][1] & O.STATUS_BAD_PARENT and got["row_status"][2] & O.STATUS_BAD_PARENT
+    assert got["row_status"][3] & O.STATUS_BAD_TOKEN
+    for b in (1, 2, 3):
+        assert got["accept_len"][b] == 0 and np.all(got["out_tokens"][b] == -1)
+    _tree_compare({k: v[:1] for k, v in got.items()}, {k: v[:1] for k, v in want.items()})
+    # A tree deeper than max_depth.
+    cfg = synth.TreeConfig("chain", 1, 8, 50, "f32", 7, 1, 1.0, 1.0, 16.0)
+    deep = synth.make_tree_inputs(cfg, seed=1)
+    deep["max_depth"] = 3
+    g = _tree_run(sv, deep, "f32")
+    assert g["row_status"][0] & O.STATUS_DEPTH_EXCEEDED
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("shuffled", [False, True])
+@pytest.mark.parametrize("with_t2d", [False, True])
+def test_d2t_scatter_matches_oracle(sv, dtype, shuffled, with_t2d):
+    import torch
+    V, Vd, R = 151936, 32000, 16
+    d2t = synth.make_d2t(5, V, Vd, shuffled=shuffled)
+    rows = np.random.default_rng(1).normal(0, 2, (R, Vd)).astype(np.float32)
+    store = synth.to_bf16_bits(rows) if dtype == "bf16" else rows
+    vals = synth.bf16_bits_to_f32(store) if dtype == "bf16" else rows
+    x = logits_tensor(store, dtype)
+    t2d = sv.build_t2d(t(d2t), V)[0] if with_t2d else None
+    out = sv.d2t_scatter(x, t(d2t), V, fill=-math.inf, t2d=t2d)
+    torch.cuda.synchronize()
+    want = O.d2t_scatter(vals, d2t, V)
+    np.testing.assert_array_equal(out.float().cpu().numpy(), want.astype(np.float32))
+
+
+def test_d2t_scatter_odd_sizes_and_fill(sv):
+    import torch
+    V, Vd, R = 1001, 37, 3
+    d2t = synth.make_d2t(2, V, Vd, shuffled=True)
+    rows = np.random.default_rng(2).normal(0, 1, (R, 40)).astype(np.float32)[:, :Vd]
+    x = t(np.ascontiguousarray(np.pad(rows, ((0, 0), (0, 3)))))[:, :Vd]  # stride 40
+    for use_t2d in (False, True):
+        t2d = sv.build_t2d(t(d2t), V)[0] if use_t2d else None
+        out = torch.empty((R, 1004), device="cuda")[:, :V]
+        sv.d2t_scatter(x, t(d2t), V, fill=-3.5, t2d=t2d, out=out)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(out.cpu().numpy(), O.d2t_scatter(rows, d2t, V, fill=-3.5))
+
+
+def test_build_t2d(sv):
+    import torch
+    d2t = synth.make_d2t(3, 151936, 32000, shuffled=True)
+    t2d, st = sv.build_t2d(t(d2t), 151936)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    np.testing.assert_array_equal(t2d.cpu().numpy(), O.build_t2d(d2t, 151936))
+    _, st = sv.build_t2d(t(np.array([1, 2, 1], np.int32)), 5)
+    assert st.item() & 2
+    _, st = sv.build_t2d(t(np.array([1, 7], np.int32)), 5)
+    assert st.item() & 1
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("V,T,top_p", [(1, 1.0, 0.9), (3, 0.5, 1.0), (1000, 0.8, 0.9), (49152, 0.8, 0.9),
+                                       (32000, 1.0, 0.95), (4097, 0.0, 1.0), (128256, 1.0, 1.0)])
+def test_sample_rows(sv, dtype, V, T, top_p):
+    import torch
+    R = 24
+    g = np.random.default_rng(V)
+    rows = g.normal(0, 2.5, (R, V)).astype(np.float32)
+    if dtype == "bf16":
+        store = synth.to_bf16_bits(rows)
+        rows = synth.bf16_bits_to_f32(store)
+    else:
+        store = rows
+    u = g.random(R, dtype=np.float32)
+    tok, prob = sv.sample(logits_tensor(store, dtype), T, top_p, t(u) if T > 0 else None)
+    torch.cuda.synchronize()
+    tok, prob = tok.cpu().numpy(), prob.cpu().numpy()
+    for r in range(R):
+        want, margin = O.sample_row(rows[r], T, top_p, float(u[r]))
+        if margin < O.NEAR:
+            continue
+        assert tok[r] == want, (r, tok[r], want, margin)
+        if T > 0:
+            p, _ = O.dist(rows[r], T, top_p)
+            assert abs(prob[r] - p[want]) <= max(1e-12, 1e-5 * p[want])
