@@ -68,6 +68,7 @@ SIGNATURES = {
     "sv_build_t2d": (_I32, [_P, _I32, _I32, _P, _P, _P]),
     "sv_sample_workspace_size": (_SZ, [ctypes.POINTER(SampleDesc)]),
     "sv_sample": (_I32, [ctypes.POINTER(SampleDesc), _P, _P, _P, _P, _P, _SZ, _P]),
+    "sv_softmax_topp": (_I32, [ctypes.POINTER(SampleDesc), _P, _P, _I64, _P, _SZ, _P]),
     "sv_status_string": (ctypes.c_char_p, [_I32]),
     "sv_version": (_I32, []),
     "sv_set_phase_events": (None, [_P, _I32]),

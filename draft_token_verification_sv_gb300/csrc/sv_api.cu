@@ -13,14 +13,19 @@ struct CallScope {
   ~CallScope() { sv::end_call(); }
 };
 
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+// Logit pointers need element alignment only (bf16: 2 bytes, fp32: 4).
+bool aligned_elem(const void* p, sv_dtype t) {
+  return (reinterpret_cast<uintptr_t>(p) & (t == SV_BF16 ? 1u : 3u)) == 0;
+}
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
 bool valid_dtype(sv_dtype t) { return t == SV_F32 || t == SV_BF16; }
 
 size_t esize(sv_dtype t) { return t == SV_BF16 ? 2 : 4; }
 
 bool valid_stride(int64_t stride, int len, sv_dtype t) {
-  return stride >= len && (static_cast<uint64_t>(stride) * esize(t)) % 16 == 0;
+  (void)t;
+  return stride >= len && stride <= (int64_t{1} << 40);
 }
 
 bool valid_vocab(int v) { return v >= 1 && v <= SV_MAX_VOCAB; }
@@ -97,13 +102,15 @@ sv_status sv_verify_chain(const sv_chain_desc* desc, const void* target_logits,
   const sv_chain_desc& d = *desc;
   if (d.batch == 0) return SV_OK;
   const bool sampling = d.temperature > 0.0f;
-  if (!target_logits || !aligned16(target_logits) || !out_tokens || !num_accepted || !workspace)
+  if (!target_logits || !aligned_elem(target_logits, d.target_dtype) || !out_tokens || !num_accepted ||
+      !workspace)
     return SV_ERR_INVALID_ARGUMENT;
   if (d.gamma > 0 && !draft_ids) return SV_ERR_INVALID_ARGUMENT;
   if (sampling) {
     if (!u_resample) return SV_ERR_INVALID_ARGUMENT;
     if (d.gamma > 0) {
-      if (!draft_logits || !aligned16(draft_logits) || !u_accept) return SV_ERR_INVALID_ARGUMENT;
+      if (!draft_logits || !aligned_elem(draft_logits, d.draft_dtype) || !u_accept)
+        return SV_ERR_INVALID_ARGUMENT;
       if ((d2t == nullptr) != (t2d == nullptr)) return SV_ERR_INVALID_ARGUMENT;
     }
   }
@@ -143,7 +150,8 @@ sv_status sv_verify_tree(const sv_tree_desc* desc, const void* logits, const int
   CallScope scope;
   if (!tree_desc_ok(desc)) return SV_ERR_INVALID_ARGUMENT;
   if (desc->batch == 0) return SV_OK;
-  if (!logits || !aligned16(logits) || !parents || !tokens || !accept_len || !path || !out_tokens ||
+  if (!logits || !aligned_elem(logits, desc->dtype) || !parents || !tokens || !accept_len || !path ||
+      !out_tokens ||
       !workspace)
     return SV_ERR_INVALID_ARGUMENT;
   if (workspace_bytes < sv_tree_workspace_size(desc)) return SV_ERR_WORKSPACE_TOO_SMALL;
@@ -161,9 +169,9 @@ sv_status sv_d2t_scatter(const void* draft_logits, int64_t in_row_stride, const 
   if (!valid_stride(in_row_stride, draft_vocab, dtype) || !valid_stride(out_row_stride, vocab, dtype))
     return SV_ERR_INVALID_ARGUMENT;
   if (rows == 0) return SV_OK;
-  if (!draft_logits || !d2t || !out || !aligned16(draft_logits) || !aligned16(out))
+  if (!draft_logits || !d2t || !out || !aligned_elem(draft_logits, dtype) || !aligned_elem(out, dtype))
     return SV_ERR_INVALID_ARGUMENT;
-  if (t2d && !aligned16(t2d)) return SV_ERR_INVALID_ARGUMENT;
+  if (t2d && !aligned4(t2d)) return SV_ERR_INVALID_ARGUMENT;
   if (static_cast<int64_t>(rows) * ((vocab + 255) / 256) > INT32_MAX) return SV_ERR_INVALID_ARGUMENT;
   return d2t_scatter(draft_logits, in_row_stride, d2t, t2d, rows, draft_vocab, vocab, dtype, fill, out,
                      out_row_stride, reinterpret_cast<cudaStream_t>(stream));
@@ -188,12 +196,24 @@ sv_status sv_sample(const sv_sample_desc* desc, const void* logits, const float*
   CallScope scope;
   if (!sample_desc_ok(desc)) return SV_ERR_INVALID_ARGUMENT;
   if (desc->rows == 0) return SV_OK;
-  if (!logits || !aligned16(logits) || !out_tokens) return SV_ERR_INVALID_ARGUMENT;
+  if (!logits || !aligned_elem(logits, desc->dtype) || !out_tokens) return SV_ERR_INVALID_ARGUMENT;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (desc->temperature == 0.0f) return greedy_sample(*desc, logits, out_tokens, out_prob, s);
   if (!u || !workspace) return SV_ERR_INVALID_ARGUMENT;
   if (workspace_bytes < sv_sample_workspace_size(desc)) return SV_ERR_WORKSPACE_TOO_SMALL;
   return sample_rows(*desc, logits, u, out_tokens, out_prob, workspace, s);
+}
+
+sv_status sv_softmax_topp(const sv_sample_desc* desc, const void* logits, float* out_probs,
+                          int64_t out_row_stride, void* workspace, size_t workspace_bytes, sv_stream_t stream) {
+  CallScope scope;
+  if (!sample_desc_ok(desc) || desc->temperature == 0.0f) return SV_ERR_INVALID_ARGUMENT;
+  if (out_row_stride < desc->vocab) return SV_ERR_INVALID_ARGUMENT;
+  if (desc->rows == 0) return SV_OK;
+  if (!logits || !aligned_elem(logits, desc->dtype) || !out_probs || !aligned4(out_probs) || !workspace)
+    return SV_ERR_INVALID_ARGUMENT;
+  if (workspace_bytes < sv_sample_workspace_size(desc)) return SV_ERR_WORKSPACE_TOO_SMALL;
+  return probs_rows(*desc, logits, out_probs, out_row_stride, workspace, reinterpret_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"
@@ -221,9 +241,13 @@ static void record_phase(cudaStream_t stream) {
   ++t_next;
 }
 
+void start_phases(cudaStream_t stream) {
+  if (t_next == 0) record_phase(stream);
+}
+
 void note_launch(cudaStream_t stream) {
   g_launches.fetch_add(1, std::memory_order_relaxed);
-  if (t_next == 0) record_phase(stream);  // events[0]: before the first launch
+  if (t_next == 0) record_phase(stream);  // a path that did not call start_phases
   record_phase(stream);
 }
 

@@ -74,6 +74,26 @@ template <> struct Elem<uint16_t> {
   }
 };
 
+// A row split into a scalar head (until the first 16-byte boundary), a body
+// of aligned 16-byte vectors and a scalar tail.
+struct RowSplit {
+  int head;  // elements before the first aligned vector
+  int nvec;  // aligned vectors
+  int tail0; // first tail element
+};
+
+template <typename E>
+__device__ __forceinline__ RowSplit split_row(const E* p, int len) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+  int head = static_cast<int>(((16u - (a & 15u)) & 15u) / sizeof(E));
+  head = min(head, len);
+  RowSplit s;
+  s.head = head;
+  s.nvec = (len - head) / Elem<E>::kPerVec;
+  s.tail0 = head + s.nvec * Elem<E>::kPerVec;
+  return s;
+}
+
 // Unpack a 16-byte vector into floats.
 template <typename E>
 __device__ __forceinline__ void unpack(const uint4& v, float* out) {

@@ -24,7 +24,8 @@ scatter_gather_kernel(const E* __restrict__ in, int64_t in_stride, const int32_t
   E* dst = out + static_cast<int64_t>(row) * out_stride;
   const int v = tile * THREADS + threadIdx.x;
   const int t0 = v * EPV;
-  if (t0 + EPV <= V) {
+  const bool vec_ok = ((reinterpret_cast<uintptr_t>(dst) | reinterpret_cast<uintptr_t>(t2d)) & 15u) == 0;
+  if (vec_ok && t0 + EPV <= V) {
     int32_t ids[EPV];
 #pragma unroll
     for (int q = 0; q < EPV / 4; ++q) {
@@ -42,7 +43,7 @@ scatter_gather_kernel(const E* __restrict__ in, int64_t in_stride, const int32_t
     }
     *reinterpret_cast<uint4*>(dst + t0) = *reinterpret_cast<const uint4*>(vals);
   } else if (t0 < V) {
-    for (int t = t0; t < V; ++t) {
+    for (int t = t0; t < min(V, t0 + EPV); ++t) {
       const int j = t2d[t];
       dst[t] = (j >= 0 && j < vd) ? src[j] : fill;
     }
@@ -63,9 +64,11 @@ scatter_fill_kernel(const E* __restrict__ in, int64_t in_stride, const int32_t* 
 #pragma unroll
   for (int e = 0; e < EPV; ++e) fv[e] = fill;
   const uint4 fvec = *reinterpret_cast<const uint4*>(fv);
-  const int nvec = V / EPV;
-  for (int v = threadIdx.x; v < nvec; v += THREADS) reinterpret_cast<uint4*>(dst)[v] = fvec;
-  for (int t = nvec * EPV + threadIdx.x; t < V; t += THREADS) dst[t] = fill;
+  const RowSplit rs = split_row(dst, V);
+  uint4* dv = reinterpret_cast<uint4*>(dst + rs.head);
+  for (int v = threadIdx.x; v < rs.nvec; v += THREADS) dv[v] = fvec;
+  for (int t = threadIdx.x; t < rs.head; t += THREADS) dst[t] = fill;
+  for (int t = rs.tail0 + threadIdx.x; t < V; t += THREADS) dst[t] = fill;
   __syncthreads();
   for (int j = threadIdx.x; j < vd; j += THREADS) {
     const int x = __ldg(d2t + j);

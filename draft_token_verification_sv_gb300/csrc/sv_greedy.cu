@@ -43,10 +43,20 @@ template <typename E, int THREADS, int UNROLL>
 __device__ __forceinline__ unsigned long long row_argmax(const E* row, int V,
                                                          unsigned long long* scratch) {
   constexpr int EPV = Elem<E>::kPerVec;
-  const int nvec = V / EPV;
-  const uint4* vp = reinterpret_cast<const uint4*>(row);
+  const RowSplit rs = split_row(row, V);
+  const int nvec = rs.nvec;
+  const uint4* vp = reinterpret_cast<const uint4*>(row + rs.head);
   float bv = -CUDART_INF_F;
   int bi = 0x7fffffff;
+  // Each thread visits its ids in increasing order (head, body, tail), so a
+  // strict '>' keeps the lowest id among equal values.
+  if (static_cast<int>(threadIdx.x) < rs.head) {
+    const float x = Elem<E>::load(row + threadIdx.x);
+    if (x > bv) {
+      bv = x;
+      bi = threadIdx.x;
+    }
+  }
   for (int v0 = threadIdx.x; v0 < nvec; v0 += THREADS * UNROLL) {
     uint4 buf[UNROLL];
 #pragma unroll
@@ -67,11 +77,11 @@ __device__ __forceinline__ unsigned long long row_argmax(const E* row, int V,
         for (int i = EPV - 1; i >= 0; --i)
           if (x[i] == vm) first = i;
         bv = vm;
-        bi = (v0 + u * THREADS) * EPV + first;
+        bi = rs.head + (v0 + u * THREADS) * EPV + first;
       }
     }
   }
-  const int tail = nvec * EPV + static_cast<int>(threadIdx.x);
+  const int tail = rs.tail0 + static_cast<int>(threadIdx.x);
   if (tail < V) {
     const float x = Elem<E>::load(row + tail);
     if (x > bv) {
@@ -275,6 +285,10 @@ sv_status greedy_chain(const sv_chain_desc& d, const void* target, const int32_t
   P.groups = d.batch;
   WorkspaceLayout L = chain_workspace_layout(d);
   P.counters = reinterpret_cast<unsigned int*>(static_cast<char*>(workspace) + L.counters);
+  // The workspace is scratch shared with other calls: clear the counters.
+  start_phases(stream);
+  if (cudaMemsetAsync(P.counters, 0, static_cast<size_t>(d.batch) * sizeof(uint32_t), stream) != cudaSuccess)
+    return SV_ERR_CUDA;
   P.g = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + L.argmax);
   P.draft_ids = ids;
   P.out_tokens = out_tokens;
@@ -297,6 +311,9 @@ sv_status greedy_tree(const sv_tree_desc& d, const void* logits, const int32_t* 
   P.rows_per_group = d.nodes;
   P.groups = d.batch;
   P.counters = static_cast<unsigned int*>(workspace);
+  start_phases(stream);
+  if (cudaMemsetAsync(P.counters, 0, static_cast<size_t>(d.batch) * sizeof(uint32_t), stream) != cudaSuccess)
+    return SV_ERR_CUDA;
   P.g = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + tree_counter_bytes(d.batch));
   P.parents = parents;
   P.tokens = tokens;

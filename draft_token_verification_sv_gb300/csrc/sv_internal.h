@@ -9,8 +9,11 @@ namespace sv {
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Call once before the first device operation of a public call: records
+// the caller's first phase event, if one is pending (sv_set_phase_events).
+void start_phases(cudaStream_t stream);
 // Call after every kernel launch: counts launches and records the caller's
-// phase event for this launch, if one is pending (see sv_set_phase_events).
+// next phase event, if one is pending.
 void note_launch(cudaStream_t stream);
 // Drop any phase events left over when a call returns.
 void end_call();
@@ -76,6 +79,8 @@ sv_status sampling_chain(const ChainArgs& a, cudaStream_t stream);
 
 sv_status sample_rows(const sv_sample_desc& d, const void* logits, const float* u,
                       int32_t* out_tokens, float* out_prob, void* workspace, cudaStream_t stream);
+sv_status probs_rows(const sv_sample_desc& d, const void* logits, float* out, int64_t out_stride,
+                     void* workspace, cudaStream_t stream);
 
 sv_status d2t_scatter(const void* in, int64_t in_stride, const int32_t* d2t, const int32_t* t2d,
                       int rows, int vd, int v, sv_dtype dtype, float fill, void* out,

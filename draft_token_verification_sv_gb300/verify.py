@@ -70,8 +70,8 @@ def _stream(stream):
 
 
 def workspace(nbytes: int, device: torch.device, stream=None) -> torch.Tensor:
-    """A zero-filled workspace of at least ``nbytes``, cached per device and
-    stream (the library leaves it zero-filled after every call)."""
+    """A device workspace of at least ``nbytes``, cached per device and
+    stream (calls on one stream run in order, so they may share it)."""
     s = stream if stream is not None else torch.cuda.current_stream(device)
     key = (device.index, s.cuda_stream)
     ws = _WORKSPACES.get(key)
@@ -224,3 +224,24 @@ def sample(logits: torch.Tensor, temperature: float, top_p: float = 1.0, u: torc
                            ctypes.c_size_t(ws.numel()), _stream(stream))
     N.check(st, "sv_sample")
     return tok, prob
+
+
+def softmax_topp(logits: torch.Tensor, temperature: float, top_p: float = 1.0, *,
+                 ws: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Filtered distribution softmax(top_p_filter(logits / T)) of every row;
+    see sv_softmax_topp.  Returns float32 [R, V]."""
+    _cuda(logits, "logits")
+    x = logits if logits.dim() == 2 else logits.reshape(-1, logits.shape[-1])
+    R, V = x.shape
+    d = N.SampleDesc()
+    d.rows, d.vocab, d.dtype = R, V, _code(x)
+    d.temperature, d.top_p = float(temperature), float(top_p)
+    d.row_stride = _row_stride(x, "logits")
+    out = torch.empty((R, V), dtype=torch.float32, device=x.device)
+    need = N.lib().sv_sample_workspace_size(ctypes.byref(d))
+    if ws is None:
+        ws = workspace(need, x.device, stream)
+    st = N.lib().sv_softmax_topp(ctypes.byref(d), _p(x), _p(out), V, _p(ws), ctypes.c_size_t(ws.numel()),
+                                 _stream(stream))
+    N.check(st, "sv_softmax_topp")
+    return out

@@ -18,10 +18,11 @@
  *   - No kernel spins on a flag or waits on another launch.
  *
  * Layouts: logits are row-major; a "row" is one position's logits over the
- * vocabulary.  Row strides are in ELEMENTS, at least the row length, and
- * stride * element size must be a multiple of 16 bytes; every logit base
- * pointer must be 16-byte aligned.  Logits may be -inf (probability 0);
- * NaN logits are not supported.
+ * vocabulary.  Row strides are in ELEMENTS and at least the row length; any
+ * such stride is accepted and logit pointers need only be aligned to their
+ * element size (rows that start on a 16-byte boundary take the vectorised
+ * path, others are read with a scalar head and tail).  Logits may be -inf
+ * (probability 0); NaN logits are not supported.
  *
  * Sources (web pages):
  *  [P3] "LLM inference acceleration in practice: draft models and
@@ -85,8 +86,9 @@ typedef struct sv_chain_desc {
 } sv_chain_desc;
 
 /* Bytes of device workspace sv_verify_chain needs for `desc`.  Returns 0 for
- * an invalid descriptor.  The workspace must be zero-filled before its first
- * use; every completed call leaves it zero-filled again. */
+ * an invalid descriptor.  The workspace is scratch: it needs no
+ * initialisation and its contents are undefined after a call.  Calls that
+ * may overlap on the device must use different workspaces. */
 size_t sv_chain_workspace_size(const sv_chain_desc* desc);
 
 /*
@@ -147,8 +149,8 @@ typedef struct sv_tree_desc {
   int64_t row_stride; /* elements between consecutive node rows */
 } sv_tree_desc;
 
-/* Workspace bytes for sv_verify_tree (zero-filled before first use; left
- * zero-filled by every completed call).  0 for an invalid descriptor. */
+/* Workspace bytes for sv_verify_tree (scratch, as for sv_verify_chain).
+ * 0 for an invalid descriptor. */
 size_t sv_tree_workspace_size(const sv_tree_desc* desc);
 
 /*
@@ -228,6 +230,17 @@ size_t sv_sample_workspace_size(const sv_sample_desc* desc);
 sv_status sv_sample(const sv_sample_desc* desc, const void* logits, const float* u,
                     int32_t* out_tokens, float* out_prob,
                     void* workspace, size_t workspace_bytes, sv_stream_t stream);
+
+/*
+ * The filtered distribution of every row: out_probs[r, j] =
+ * softmax(top_p_filter(logits[r] / T))[j], with the same top-p rule and tie
+ * order as sv_verify_chain ([P3] §4.2: _apply_top_p, then F.softmax).
+ * T must be > 0.  logits [R] rows of V (desc->row_stride); out_probs [R]
+ * rows of V float (out_row_stride >= V); workspace as for sv_sample.
+ */
+sv_status sv_softmax_topp(const sv_sample_desc* desc, const void* logits, float* out_probs,
+                          int64_t out_row_stride, void* workspace, size_t workspace_bytes,
+                          sv_stream_t stream);
 
 /*
  * Profiling hooks (host-side; they add no device work).

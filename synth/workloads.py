@@ -221,7 +221,9 @@ def make_tree_inputs(cfg: TreeConfig, seed: int | None = None, *, batch: int | N
                 planted[par] = t
                 logits[b, par, t] += np.float32(cfg.plant_spike)
             else:
-                while True:
+                # Distinct sibling tokens while the vocabulary allows it (a few
+                # tries); tiny vocabularies fall back to a repeated token.
+                for _ in range(64):
                     t = int(g_t.integers(V))
                     if t not in used[par] and t != planted[par]:
                         break

@@ -85,7 +85,7 @@ int main(void) {
 # Fake, 16-byte aligned "device" addresses: validation must reject the call
 # before anything could dereference them.
 A = ctypes.c_void_p(0x100000)
-MIS = ctypes.c_void_p(0x100004)
+MIS = ctypes.c_void_p(0x100001)  # not even 2-byte aligned
 
 
 def _chain(N, **kw):
@@ -111,8 +111,8 @@ def _call_chain(N, d, ws_bytes=1 << 30, **ptr):
 @pytest.mark.parametrize("field,value", [
     ("gamma", 65), ("gamma", -1), ("batch", -1), ("vocab", 0), ("vocab", (1 << 24) + 1),
     ("top_p", 0.0), ("top_p", 1.5), ("top_p", float("nan")), ("temperature", -0.5),
-    ("temperature", float("inf")), ("target_row_stride", 999), ("target_row_stride", 1001),
-    ("draft_row_stride", 1002), ("target_dtype", 7), ("draft_vocab", 999),
+    ("temperature", float("inf")), ("target_row_stride", 999), ("target_row_stride", -4),
+    ("draft_row_stride", 999), ("target_dtype", 7), ("draft_vocab", 999),
 ])
 def test_chain_rejects_bad_descriptor(N, field, value):
     assert _call_chain(N, _chain(N, **{field: value})) == N.SV_ERR_INVALID_ARGUMENT
@@ -173,7 +173,7 @@ def _tree(N, **kw):
 
 
 @pytest.mark.parametrize("field,value", [("nodes", 0), ("nodes", 1025), ("max_depth", -1),
-                                         ("max_depth", 65), ("row_stride", 1004), ("vocab", 0)])
+                                         ("max_depth", 65), ("row_stride", 999), ("vocab", 0)])
 def test_tree_rejects_bad_descriptor(N, field, value):
     d = _tree(N, **{field: value})
     assert N.lib().sv_verify_tree(ctypes.byref(d), A, A, A, A, A, A, None, A, ctypes.c_size_t(1 << 30),
@@ -194,7 +194,8 @@ def test_scatter_and_t2d_checks(N):
     f = N.lib().sv_d2t_scatter
     E = N.SV_ERR_INVALID_ARGUMENT
     assert f(A, 32, A, None, 2, 32, 16, N.SV_F32, -1.0, A, 16, None) == E   # draft_vocab > vocab
-    assert f(A, 30, A, None, 2, 30, 64, N.SV_F32, -1.0, A, 64, None) == E   # stride not 16-byte
+    assert f(A, 30, A, None, 2, 32, 64, N.SV_F32, -1.0, A, 64, None) == E   # in stride < draft_vocab
+    assert f(A, 32, A, None, 2, 32, 64, N.SV_F32, -1.0, A, 60, None) == E   # out stride < vocab
     assert f(A, 32, None, None, 2, 32, 64, N.SV_F32, -1.0, A, 64, None) == E
     assert f(MIS, 32, A, None, 2, 32, 64, N.SV_F32, -1.0, A, 64, None) == E
     assert f(A, 32, A, None, 0, 32, 64, N.SV_F32, -1.0, A, 64, None) == N.SV_OK  # no rows

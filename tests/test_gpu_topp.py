@@ -1,0 +1,113 @@
+"""The filtered distribution softmax(top_p_filter(l / T)) on the GPU against
+the fp64 oracle, element by element: random rows over the pages' vocabulary
+sizes, and rows built to reach every branch of the threshold search (the
+common binned path, a candidate list overflow, a cut among masses below
+2^-30, and a tie group of more than 64 equal logits at the cut)."""
+import numpy as np
+import pytest
+
+import synth
+from oracle import sv_oracle as O
+
+from _parity import TOL, logits_tensor
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def sv():
+    import __graft_entry__
+    __graft_entry__.build()
+    import draft_token_verification_sv_gb300 as sv
+    return sv
+
+
+def _check(sv, rows, dtype, T, top_p, tie_index=None):
+    import torch
+    if dtype == "bf16":
+        store = synth.to_bf16_bits(rows)
+        rows = synth.bf16_bits_to_f32(store)
+    else:
+        store = np.ascontiguousarray(rows, dtype=np.float32)
+        rows = store
+    got = sv.softmax_topp(logits_tensor(store, dtype), T, top_p)
+    torch.cuda.synchronize()
+    got = got.cpu().numpy().astype(np.float64)
+    near = 0
+    for r in range(rows.shape[0]):
+        want, margin = O.dist(rows[r], T, top_p)
+        if margin < O.NEAR:
+            # The cut is within 1e-6 of top_p: the kept sets may differ at
+            # the boundary only; the probabilities of common ids still agree
+            # up to the kept mass they are normalised by.
+            near += 1
+            both = (got[r] > 0) & (want > 0)
+            pi, _ = O.dist(rows[r], T, 1.0)          # unfiltered softmax
+            differ = (got[r] > 0) != (want > 0)
+            assert pi[differ].sum() <= 2e-6, pi[differ].sum()
+            scale = got[r][both].sum() / want[both].sum()
+            np.testing.assert_allclose(got[r][both], want[both] * scale, rtol=TOL[dtype], atol=1e-12)
+            continue
+        same_set = ((got[r] > 0) == (want > 0)) | (want < 1e-30)
+        assert same_set.all(), (r, np.nonzero(~same_set)[0][:10])
+        ok = np.abs(got[r] - want) <= np.maximum(1e-12, TOL[dtype] * want)
+        assert ok.all(), (r, np.nonzero(~ok)[0][:5], got[r][~ok][:5], want[~ok][:5])
+    return near
+
+
+@pytest.mark.parametrize("V,dtype,T,top_p", [
+    (1, "f32", 1.0, 0.5), (7, "bf16", 0.7, 0.9), (1000, "f32", 0.8, 0.9), (4097, "bf16", 1.3, 0.5),
+    (32000, "f32", 1.0, 0.95), (49152, "bf16", 0.8, 0.9), (128256, "bf16", 1.0, 0.99),
+    (151936, "f32", 1.0, 0.95), (151936, "f32", 0.5, 0.1), (50257, "bf16", 1.0, 0.9),
+])
+def test_random_rows(sv, V, dtype, T, top_p):
+    g = np.random.default_rng(V + int(top_p * 100))
+    R = 12
+    rows = g.normal(0, 2.5, (R, V)).astype(np.float32)
+    rows[::3] *= 4.0          # some peaked rows
+    rows[1::4] = np.round(rows[1::4])  # some with many ties
+    _check(sv, rows, dtype, T, top_p)
+
+
+def test_candidate_overflow_path(sv):
+    """Nearly all logits equal: the cut bin holds far more than one block's
+    candidate list, so the exact generic select runs."""
+    g = np.random.default_rng(1)
+    rows = np.zeros((4, 30000), np.float32)
+    for r in range(4):
+        rows[r, g.choice(30000, 10, replace=False)] = 1.0
+    _check(sv, rows, "f32", 1.0, 0.49991)
+    _check(sv, rows, "bf16", 1.0, 0.3)
+
+
+def test_cut_among_tiny_masses(sv):
+    """One dominant logit and a long tail below 2^-30.5 of its mass: with
+    top_p close to 1 the cut falls in the open bin."""
+    rows = np.full((3, 150000), -21.5, np.float32)
+    rows[:, 17] = 0.0
+    rows[1, 100:200] = -21.0
+    _check(sv, rows, "bf16", 1.0, 0.99999)
+    _check(sv, rows, "f32", 1.0, 0.99999)
+
+
+def test_large_tie_group_at_cut(sv):
+    """More than 64 equal logits straddle the cut: the tie group is cut by
+    index."""
+    g = np.random.default_rng(2)
+    rows = np.full((4, 50000), -3.0, np.float32)
+    for r in range(4):
+        idx = g.permutation(50000)
+        rows[r, idx[:100]] = 5.0
+        rows[r, idx[100:1100]] = 4.0
+    for top_p in (0.3, 0.6, 0.9):
+        _check(sv, rows, "bf16", 1.0, top_p)
+        _check(sv, rows, "f32", 1.0, top_p)
+
+
+def test_unaligned_rows(sv):
+    """Rows whose start is not 16-byte aligned (odd row length, packed)."""
+    g = np.random.default_rng(3)
+    for V in (1001, 32003, 151937):
+        rows = g.normal(0, 2, (5, V)).astype(np.float32)
+        _check(sv, rows, "f32", 0.9, 0.9)
+        _check(sv, rows, "bf16", 0.9, 0.9)
