@@ -187,7 +187,7 @@ sv_status sv_build_t2d(const int32_t* d2t, int32_t draft_vocab, int32_t vocab, i
 
 size_t sv_sample_workspace_size(const sv_sample_desc* desc) {
   if (!sample_desc_ok(desc)) return 0;
-  return align_up(static_cast<size_t>(desc->rows) * sizeof(RowStats), 256) + 256;
+  return sample_workspace_bytes(*desc);
 }
 
 sv_status sv_sample(const sv_sample_desc* desc, const void* logits, const float* u,

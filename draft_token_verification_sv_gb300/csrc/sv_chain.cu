@@ -126,25 +126,24 @@ static sv_status launch_stream(const StatsLaunch& L, int rows, cudaStream_t stre
 }
 
 // One launch when both row sets share a dtype, else one per set.  top_p < 1
-// selects the cluster-resident top-p kernel.
-static sv_status launch_stats_sets(StatsLaunch L, sv_dtype d0, sv_dtype d1, bool topp, int max_len,
+// selects the top-p kernel, whose scratch follows the row statistics.
+static sv_status launch_stats_sets(StatsLaunch L, sv_dtype d0, sv_dtype d1, bool topp, void* scratch,
                                    cudaStream_t stream) {
-  auto one = [&](const StatsLaunch& X, sv_dtype dt, int rows, int len) -> sv_status {
-    if (topp) return launch_topp_stats(X, rows, len, dt, stream);
+  auto one = [&](const StatsLaunch& X, sv_dtype dt, void* scr) -> sv_status {
+    if (topp) return launch_topp_stats(X, dt, scr, stream);
+    const int rows = X.set[0].rows + (X.nsets > 1 ? X.set[1].rows : 0);
     return dt == SV_BF16 ? launch_stream<uint16_t>(X, rows, stream) : launch_stream<float>(X, rows, stream);
   };
-  // The top-p kernel sizes its clusters by the row length, so row sets of
-  // different lengths (EAGLE3 draft rows) get launches of their own.
-  const bool same_len = L.nsets == 1 || L.set[0].len == L.set[1].len;
-  if (L.nsets == 1 || (d0 == d1 && (!topp || same_len)))
-    return one(L, d0, L.set[0].rows + (L.nsets > 1 ? L.set[1].rows : 0), max_len);
+  if (L.nsets == 1 || d0 == d1) return one(L, d0, scratch);
   StatsLaunch a = L, b = L;
   a.nsets = 1;
   b.nsets = 1;
   b.set[0] = L.set[1];
-  sv_status s = one(a, d0, a.set[0].rows, a.set[0].len);
+  sv_status s = one(a, d0, scratch);
   if (s != SV_OK) return s;
-  return one(b, d1, b.set[0].rows, b.set[0].len);
+  void* scr_b = topp ? static_cast<char*>(scratch) + topp_scratch_bytes(a.set[0].rows, a.set[0].len, 0, 0)
+                     : scratch;
+  return one(b, d1, scr_b);
 }
 
 static float log2e_over(double T) { return static_cast<float>(1.4426950408889634 / T); }
@@ -192,7 +191,8 @@ sv_status sampling_chain(const ChainArgs& a, cudaStream_t stream) {
     max_len = std::max(max_len, d.draft_vocab);
   }
   start_phases(stream);
-  sv_status s = launch_stats_sets(L, d.target_dtype, d.draft_dtype, resident, max_len, stream);
+  void* scratch = static_cast<char*>(a.workspace) + WL.topp;
+  sv_status s = launch_stats_sets(L, d.target_dtype, d.draft_dtype, resident, scratch, stream);
   if (s != SV_OK) return s;
   DecideParams P{};
   P.target = a.target;
@@ -238,7 +238,8 @@ sv_status sample_rows(const sv_sample_desc& d, const void* logits, const float* 
   T.vocab = d.vocab;
   T.out = stats;
   start_phases(stream);
-  sv_status s = launch_stats_sets(L, d.dtype, d.dtype, d.top_p < 1.0f, d.vocab, stream);
+  void* scratch = static_cast<char*>(workspace) + sample_stats_bytes(d.rows);
+  sv_status s = launch_stats_sets(L, d.dtype, d.dtype, d.top_p < 1.0f, scratch, stream);
   if (s != SV_OK) return s;
   DecideParams P{};
   P.target = logits;
@@ -304,7 +305,8 @@ sv_status probs_rows(const sv_sample_desc& d, const void* logits, float* out, in
   T.vocab = d.vocab;
   T.out = stats;
   start_phases(stream);
-  sv_status s = launch_stats_sets(L, d.dtype, d.dtype, d.top_p < 1.0f, d.vocab, stream);
+  void* scratch = static_cast<char*>(workspace) + sample_stats_bytes(d.rows);
+  sv_status s = launch_stats_sets(L, d.dtype, d.dtype, d.top_p < 1.0f, scratch, stream);
   if (s != SV_OK) return s;
   const int tiles = (d.vocab + 2047) / 2048;
   const unsigned grid = static_cast<unsigned>(d.rows) * tiles;

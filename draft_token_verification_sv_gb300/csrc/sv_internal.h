@@ -28,9 +28,13 @@ struct FuncAttrCache {
   bool ensure(const void* func, size_t dyn_smem, bool non_portable_cluster);
 };
 
+// Scratch of the top-p statistics kernel for two row sets (sv_topp.cu).
+size_t topp_scratch_bytes(int rows0, int len0, int rows1, int len1);
+
 // Chain workspace: [counters: B u32][stats: B(2γ+1) RowStats][argmax: B(γ+1) i32]
+//                  [top-p scratch when T > 0 and top_p < 1]
 struct WorkspaceLayout {
-  size_t counters, stats, argmax, total;
+  size_t counters, stats, argmax, topp, total;
 };
 
 inline WorkspaceLayout chain_workspace_layout(const sv_chain_desc& d) {
@@ -40,8 +44,19 @@ inline WorkspaceLayout chain_workspace_layout(const sv_chain_desc& d) {
   L.counters = 0;
   L.stats = align_up(B * sizeof(uint32_t), 256);
   L.argmax = L.stats + align_up(B * (2 * G + 1) * sizeof(RowStats), 256);
-  L.total = L.argmax + align_up(B * (G + 1) * sizeof(int32_t), 256);
+  L.topp = L.argmax + align_up(B * (G + 1) * sizeof(int32_t), 256);
+  L.total = L.topp;
+  if (d.temperature > 0.0f && d.top_p < 1.0f)
+    L.total += topp_scratch_bytes(d.batch * (d.gamma + 1), d.vocab, d.batch * d.gamma, d.draft_vocab);
   return L;
+}
+
+// Draft-side sampling / filtered probabilities: [stats: R RowStats][top-p scratch]
+inline size_t sample_stats_bytes(int rows) { return align_up(static_cast<size_t>(rows) * sizeof(RowStats), 256); }
+inline size_t sample_workspace_bytes(const sv_sample_desc& d) {
+  size_t n = sample_stats_bytes(d.rows);
+  if (d.temperature > 0.0f && d.top_p < 1.0f) n += topp_scratch_bytes(d.rows, d.vocab, 0, 0);
+  return n + 256;
 }
 
 inline size_t tree_counter_bytes(int batch) {

@@ -28,7 +28,9 @@ struct StatsLaunch {
   int nsets;
   float c;             // log2(e) / T
   float top_p;
-  int cl;              // cluster size (top-p kernel)
+  int nslices[2];      // top-p kernel: slices per row of each set
+  float* summ;         // top-p kernel: per-slice summaries
+  unsigned* counters;  // top-p kernel: finished slices per row
 };
 
 __device__ __forceinline__ const RowSet& pick_set(const StatsLaunch& L, int& r) {
@@ -89,7 +91,8 @@ struct DecideParams {
 
 sv_status launch_decide(const DecideParams& P, sv_dtype target_dtype, sv_dtype draft_dtype, cudaStream_t stream);
 
-// Top-p statistics of every row of L (sv_topp.cu); rows of at most max_len.
-sv_status launch_topp_stats(const StatsLaunch& L, int rows, int max_len, sv_dtype dtype, cudaStream_t stream);
+// Top-p statistics of every row of L (sv_topp.cu), with `scratch` of
+// topp_scratch_bytes(...) bytes (slice summaries and row counters).
+sv_status launch_topp_stats(StatsLaunch L, sv_dtype dtype, void* scratch, cudaStream_t stream);
 
 }  // namespace sv
