@@ -62,6 +62,9 @@ SIGNATURES = {
     "sv_chain_workspace_size": (_SZ, [ctypes.POINTER(ChainDesc)]),
     "sv_verify_chain": (_I32, [ctypes.POINTER(ChainDesc), _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                _P, _P, _SZ, _P]),
+    "sv_verify_chain_static": (_I32, [ctypes.POINTER(ChainDesc), _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                      _P, _P, _P]),
+    "sv_static_scratch_bytes": (_SZ, []),
     "sv_tree_workspace_size": (_SZ, [ctypes.POINTER(TreeDesc)]),
     "sv_verify_tree": (_I32, [ctypes.POINTER(TreeDesc), _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "sv_d2t_scatter": (_I32, [_P, _I64, _P, _P, _I32, _I32, _I32, _I32, _F, _P, _I64, _P]),

@@ -140,6 +140,40 @@ sv_status sv_verify_chain(const sv_chain_desc* desc,
                           float* p_draft, float* q_draft, int32_t* row_status,
                           void* workspace, size_t workspace_bytes, sv_stream_t stream);
 
+/*
+ * sv_verify_chain for callers that cannot allocate device memory (for
+ * example code that runs inside another runtime's allocator, or a serving
+ * loop that forbids allocations after warm-up).  The pages have no
+ * counterpart to this entry point: it is a deployment convenience.
+ *
+ * Same arguments and results as sv_verify_chain, without the workspace: the
+ * scratch is an array of sv_static_scratch_bytes() bytes (16 MiB) built into
+ * the library, which every GPU that loads the library keeps until the
+ * process exits.  Nothing is allocated and no allocating routine is called.
+ *   - A descriptor that needs more scratch than the array holds
+ *     (sv_chain_workspace_size(desc) > sv_static_scratch_bytes()) is rejected
+ *     with SV_ERR_WORKSPACE_TOO_SMALL before anything runs.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current) and caches it; make that first call outside any
+ *     stream capture.
+ *   - All calls on a device share the one array, which keeps whatever the
+ *     last call left in it.  The verify path needs no zeroed scratch (it
+ *     clears its own counters on every call).  Calls that may overlap on the
+ *     GPU (different streams, no ordering between them) race on the array:
+ *     order them, or use sv_verify_chain with separate workspaces.
+ */
+sv_status sv_verify_chain_static(const sv_chain_desc* desc,
+                                 const void* target_logits, const void* draft_logits,
+                                 const int32_t* d2t, const int32_t* t2d,
+                                 const int32_t* draft_ids,
+                                 const float* u_accept, const float* u_resample,
+                                 int32_t* out_tokens, int32_t* num_accepted,
+                                 float* p_draft, float* q_draft, int32_t* row_status,
+                                 sv_stream_t stream);
+
+/* Size in bytes of the scratch array used by sv_verify_chain_static. */
+size_t sv_static_scratch_bytes(void);
+
 typedef struct sv_tree_desc {
   int32_t batch;      /* B >= 0 trees */
   int32_t nodes;      /* N in [1, SV_MAX_TREE_NODES] nodes per tree, node 0 = root */
