@@ -215,7 +215,7 @@ sv_status sampling_chain(const ChainArgs& a, cudaStream_t stream) {
   P.p_draft = a.p_draft;
   P.q_draft = a.q_draft;
   P.row_status = a.row_status;
-  return launch_decide(P, d.target_dtype, d.draft_dtype, stream);
+  return launch_decide(P, d.target_dtype, d.draft_dtype, static_cast<char*>(a.workspace) + WL.decide, stream);
 }
 
 sv_status sample_rows(const sv_sample_desc& d, const void* logits, const float* u,
@@ -253,7 +253,8 @@ sv_status sample_rows(const sv_sample_desc& d, const void* logits, const float* 
   P.u_resample = u;
   P.out_tokens = out_tokens;
   P.out_prob = out_prob;
-  return launch_decide(P, d.dtype, d.dtype, stream);
+  return launch_decide(P, d.dtype, d.dtype,
+                       static_cast<char*>(workspace) + sample_stats_bytes(d.rows) + sample_topp_bytes(d), stream);
 }
 
 }  // namespace sv

@@ -7,57 +7,25 @@
 // acceptances sample the extra token from p) and §4.2 (the accept loop of
 // generate()).  The uniforms are supplied by the caller.
 //
-// One thread-block cluster per batch row.  Every block evaluates the
-// decisions (a few scalars per row, from the statistics pass), then draws
-// over its own contiguous segment of the vocabulary: per 4096-id chunk it
-// sums the draw weights (8 contiguous ids per thread, 16-byte loads).  The
-// segment totals are exchanged through distributed shared memory; the block
-// whose segment holds u * total rescans the one chunk that holds it with a
-// block-wide prefix scan and writes the row's outputs.
+// The vocabulary of a batch row is cut into segments of NC chunks of 2048
+// ids, one thread block per (row, segment), with no cooperation between the
+// blocks of a row while they stream.  Every block first evaluates the row's
+// decisions (a few scalars per draft, from the statistics pass) to learn the
+// draw position k, then loads its segment of target row k (and of draft row
+// k when drawing from the residual) with every 16-byte load of the segment
+// issued before the first is used, and writes one draw-weight sum per chunk.
+// The last block of the row to finish (a counter per row) scans the chunk
+// sums, finds the chunk that holds u * total and rescans that one chunk
+// (from L2) with a block-wide prefix scan to pick the token.
 #include "sv_rows.cuh"
 
 namespace sv {
 
-constexpr int kDThreads = 512;
-constexpr int kDEPT = 8;
-constexpr int kDChunk = kDThreads * kDEPT;
-
-struct DecideShared {
-  float red[32];
-  double scan[32];
-  double seg_total;
-  int seg_last;
-  unsigned char acc[SV_MAX_GAMMA];
-  int k;
-  unsigned status;
-  int writer;
-  int tok;
-  int chunk;
-  double carry;
-  double target;
-};
-
-// Eight consecutive logits starting at j0 (a multiple of 8); -inf past V.
-template <typename E>
-__device__ __forceinline__ void load8(const E* row, int j0, int V, bool aligned, float* out) {
-  if (aligned && j0 + 8 <= V) {
-    if constexpr (sizeof(E) == 2) {
-      const uint4 w = ldg_stream(row + j0);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) out[e] = Elem<uint16_t>::at(w, e);
-    } else {
-      const uint4 a = ldg_stream(row + j0), b = ldg_stream(row + j0 + 4);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        out[e] = Elem<float>::at(a, e);
-        out[e + 4] = Elem<float>::at(b, e);
-      }
-    }
-  } else {
-#pragma unroll
-    for (int e = 0; e < 8; ++e) out[e] = j0 + e < V ? Elem<E>::load(row + j0 + e) : -CUDART_INF_F;
-  }
-}
+constexpr int kDThreads = 256;
+constexpr int kDEPT = 8;                    // consecutive ids per thread per chunk
+constexpr int kDChunk = kDThreads * kDEPT;  // 2048 ids per chunk
+constexpr int kDWarps = kDThreads / 32;
+constexpr int kDMaxNC = 8;                  // chunks per block: 8 for two bf16 rows, else 4
 
 struct DrawSide {
   float mc, invK;
@@ -65,283 +33,459 @@ struct DrawSide {
   int32_t cut;
 };
 
-// Draw weights of ids j0..j0+7: p(j) (bonus) or max(0, p(j) - q(j)).
-template <typename ET, typename ED>
-__device__ __forceinline__ void weights8(const ET* trow, const ED* drow, const int32_t* t2d, int V, int Vd,
-                                         bool t_al, bool d_al, bool resid, float c, const DrawSide& pt,
-                                         const DrawSide& pd, int j0, float* w) {
-  float lt[8];
-  load8<ET>(trow, j0, V, t_al, lt);
+struct DecideShared {
+  float wsum[kDMaxNC][kDWarps];
+  DrawSide pt, pd;
+  double scan[32];
+  int red_i[32];
+  int k;
+  unsigned status;
+  int last;
+  int chunk;
+  int tok;
+  int best;
+  double carry;
+  double target;
+  double total;
+};
+
+// Raw 16-byte vectors of 8 consecutive logits: one for bf16, two for f32.
+template <typename E>
+struct Raw8 {
+  static constexpr int kVec = sizeof(E) == 2 ? 1 : 2;
+  uint4 v[kVec];
+};
+
+template <typename E>
+__device__ __forceinline__ void raw_load(Raw8<E>& r, const E* p) {
 #pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    const int j = j0 + e;
-    w[e] = (j < V && kept(order_key(lt[e]), j, pt.tau, pt.cut)) ? weight(lt[e], c, pt.mc) * pt.invK : 0.0f;
-  }
-  if (!resid) return;
-  float ld[8];
-  if (t2d) {
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const int j = j0 + e;
-      const int jd = j < V ? __ldg(t2d + j) : -1;
-      ld[e] = (jd >= 0 && jd < Vd) ? Elem<ED>::load(drow + jd) : -CUDART_INF_F;
-    }
+  for (int i = 0; i < Raw8<E>::kVec; ++i) r.v[i] = __ldcg(reinterpret_cast<const uint4*>(p) + i);
+}
+
+template <typename E>
+__device__ __forceinline__ float raw_at(const Raw8<E>& r, int e) {
+  if constexpr (sizeof(E) == 2) {
+    return Elem<uint16_t>::at(r.v[0], e);
   } else {
-    load8<ED>(drow, j0, V, d_al, ld);
-  }
-#pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    const int j = j0 + e;
-    const float q = (ld[e] > -CUDART_INF_F && kept(order_key(ld[e]), j, pd.tau, pd.cut))
-                        ? weight(ld[e], c, pd.mc) * pd.invK
-                        : 0.0f;
-    w[e] = fmaxf(0.0f, w[e] - q);
+    return Elem<float>::at(r.v[e >> 2], e & 3);
   }
 }
 
+__device__ __forceinline__ DrawSide draw_side(const RowStats& s) {
+  return DrawSide{s.mc, s.K > 0.0 ? static_cast<float>(1.0 / s.K) : 0.0f, s.tau, s.cut};
+}
+
+// Normalised filtered probability of id j with logit x (0 if filtered out).
+__device__ __forceinline__ float prob_of(float x, int j, float c, const DrawSide& s) {
+  if (s.tau != 0u && !kept(order_key(x), j, s.tau, s.cut)) return 0.0f;
+  return weight(x, c, s.mc) * s.invK;
+}
+
+// Draw weight of id j: p(j) (bonus) or max(0, p(j) - q(j)) (residual; ld is
+// -inf where the draft row has no entry for j).
+__device__ __forceinline__ float draw_weight(float lt, float ld, int j, bool resid, float c, const DrawSide& pt,
+                                             const DrawSide& pd) {
+  const float p = prob_of(lt, j, c, pt);
+  if (!resid) return p;
+  const float q = ld > -CUDART_INF_F ? prob_of(ld, j, c, pd) : 0.0f;
+  return fmaxf(0.0f, p - q);
+}
+
+struct RowView {
+  const void* trow;
+  const void* drow;
+  bool fast;  // 16-byte aligned rows and V a multiple of 8: whole-vector loads
+};
+
+// Draw weights of the 8 ids of chunk `ch` owned by this thread (any layout).
 template <typename ET, typename ED>
-__global__ void __launch_bounds__(kDThreads) decide_kernel(DecideParams P, int cld) {
-  extern __shared__ float chunk_sums[];
+__device__ __forceinline__ void chunk_weights(const DecideParams& P, const RowView& R, int ch, bool resid,
+                                              const DrawSide& pt, const DrawSide& pd, float* w) {
+  const int j0 = ch * kDChunk + static_cast<int>(threadIdx.x) * kDEPT;
+  const ET* trow = static_cast<const ET*>(R.trow);
+  const ED* drow = static_cast<const ED*>(R.drow);
+  float lt[8], ld[8];
+  if (R.fast && j0 < P.V) {
+    Raw8<ET> rt;
+    raw_load(rt, trow + j0);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) lt[e] = raw_at(rt, e);
+    if (resid && !P.t2d) {
+      Raw8<ED> rd;
+      raw_load(rd, drow + j0);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) ld[e] = raw_at(rd, e);
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) lt[e] = j0 + e < P.V ? Elem<ET>::load(trow + j0 + e) : -CUDART_INF_F;
+    if (resid && !P.t2d) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) ld[e] = j0 + e < P.V ? Elem<ED>::load(drow + j0 + e) : -CUDART_INF_F;
+    }
+  }
+  if (resid && P.t2d) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const int jd = j0 + e < P.V ? __ldg(P.t2d + j0 + e) : -1;
+      ld[e] = (jd >= 0 && jd < P.Vd) ? Elem<ED>::load(drow + jd) : -CUDART_INF_F;
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < 8; ++e)
+    w[e] = j0 + e < P.V ? draw_weight(lt[e], resid ? ld[e] : -CUDART_INF_F, j0 + e, resid, P.c, pt, pd) : 0.0f;
+}
+
+// Per-thread draw-weight sums of the NC chunks c0.. of this block with every
+// load of the segment in flight together (R.fast only); groups of 8 ids past
+// the row add nothing.  lp: the largest id with a positive weight.
+template <typename ET, typename ED, int NC>
+__device__ __forceinline__ void segment_sums_fast(const DecideParams& P, const RowView& R, int c0, bool resid,
+                                                  const DrawSide& pt, const DrawSide& pd, float* part, int& lp) {
+  const ET* trow = static_cast<const ET*>(R.trow);
+  const ED* drow = static_cast<const ED*>(R.drow);
+  const int tj = static_cast<int>(threadIdx.x) * kDEPT;
+  Raw8<ET> rt[NC];
+  bool ok[NC];
+#pragma unroll
+  for (int q = 0; q < NC; ++q) {
+    const int j0 = (c0 + q) * kDChunk + tj;
+    ok[q] = j0 < P.V;  // V is a multiple of 8: a group is wholly in or out
+    raw_load(rt[q], trow + (ok[q] ? j0 : 0));
+  }
+  float ld[NC][8];
+  if (resid) {
+    if (P.t2d) {
+      int4 m[NC][2];
+#pragma unroll
+      for (int q = 0; q < NC; ++q) {
+        const int4* src = reinterpret_cast<const int4*>(P.t2d + (ok[q] ? (c0 + q) * kDChunk + tj : 0));
+        m[q][0] = __ldg(src);
+        m[q][1] = __ldg(src + 1);
+      }
+#pragma unroll
+      for (int q = 0; q < NC; ++q) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int4& v = m[q][e >> 2];
+          const int jd = (e & 3) == 0 ? v.x : (e & 3) == 1 ? v.y : (e & 3) == 2 ? v.z : v.w;
+          ld[q][e] = (jd >= 0 && jd < P.Vd) ? Elem<ED>::load(drow + jd) : -CUDART_INF_F;
+        }
+      }
+    } else {
+      Raw8<ED> rd[NC];
+#pragma unroll
+      for (int q = 0; q < NC; ++q) raw_load(rd[q], drow + (ok[q] ? (c0 + q) * kDChunk + tj : 0));
+#pragma unroll
+      for (int q = 0; q < NC; ++q) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) ld[q][e] = raw_at(rd[q], e);
+      }
+    }
+  }
+#pragma unroll
+  for (int q = 0; q < NC; ++q) {
+    const int j0 = (c0 + q) * kDChunk + tj;
+    float s = 0.0f;
+    if (ok[q]) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float w = draw_weight(raw_at(rt[q], e), resid ? ld[q][e] : -CUDART_INF_F, j0 + e, resid, P.c, pt, pd);
+        s += w;
+        if (w > 0.0f) lp = j0 + e;
+      }
+    }
+    part[q] = s;
+  }
+}
+
+// Block sum of one float per thread; the result is valid in thread 0.
+__device__ __forceinline__ float block_sum_to0(float v, DecideShared& sh) {
+  v = warp_sum(v);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __syncthreads();
+  if (lane == 0) sh.wsum[0][warp] = v;
+  __syncthreads();
+  float s = 0.0f;
+  if (threadIdx.x == 0)
+    for (int w = 0; w < kDWarps; ++w) s += sh.wsum[0][w];
+  return s;
+}
+
+template <typename ET, typename ED, int NC>
+__global__ void __launch_bounds__(kDThreads, 2) decide_kernel(DecideParams P, int nseg) {
   __shared__ DecideShared sh;
-  cg::cluster_group cluster = cg::this_cluster();
-  const int rank = static_cast<int>(cluster.block_rank());
-  const int b = blockIdx.x / cld;
-  const int tid = threadIdx.x;
-  const int G = P.G;
+  const int b = blockIdx.x / nseg;
+  const int seg = blockIdx.x - b * nseg;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = P.G, V = P.V;
+  const int nchunks = (V + kDChunk - 1) / kDChunk;
   const RowStats* ts = P.t_stats + static_cast<int64_t>(b) * (G + 1);
   const RowStats* ds = P.d_stats + static_cast<int64_t>(b) * G;
-  if (tid == 0) sh.status = 0;
-  __syncthreads();
-  // Decisions (identical in every block of the cluster).
-  for (int i = tid; i <= G; i += kDThreads) {
-    uint32_t st = ts[i].status;
-    if (i < G) {
-      st |= ds[i].status;
-      const int x = P.ids[static_cast<int64_t>(b) * G + i];
-      if (x < 0 || x >= P.V) st |= SV_ROW_BAD_DRAFT_ID;
-      const double p = ts[i].K > 0.0 ? static_cast<double>(ts[i].e_query) / ts[i].K : 0.0;
-      const double q = ds[i].K > 0.0 ? static_cast<double>(ds[i].e_query) / ds[i].K : 0.0;
-      const double u = static_cast<double>(P.u_accept[static_cast<int64_t>(b) * G + i]);
-      sh.acc[i] = (u * q < p) ? 1 : 0;
-      if (rank == 0 && P.p_draft) P.p_draft[static_cast<int64_t>(b) * G + i] = static_cast<float>(p);
-      if (rank == 0 && P.q_draft) P.q_draft[static_cast<int64_t>(b) * G + i] = static_cast<float>(q);
+
+  // Decisions (identical in every block of the row), by warp 0: accept
+  // draft i iff u_i * q_i < p_i, with p = e_query / K on each side (compared
+  // as u * e_q * K_t < e_t * K_d, both K > 0, to avoid divisions).
+  if (warp == 0) {
+    uint32_t st = 0;
+    int k = G;
+    for (int base = 0; base <= G; base += 32) {
+      const int i = base + lane;
+      bool rej = false;
+      if (i <= G) {
+        const RowStats t = ts[i];
+        st |= t.status;
+        if (i < G) {
+          const RowStats d = ds[i];
+          st |= d.status;
+          const int x = P.ids[static_cast<int64_t>(b) * G + i];
+          if (x < 0 || x >= V) st |= SV_ROW_BAD_DRAFT_ID;
+          const double u = static_cast<double>(P.u_accept[static_cast<int64_t>(b) * G + i]);
+          const double et = t.K > 0.0 ? static_cast<double>(t.e_query) : 0.0;
+          const double eq = d.K > 0.0 ? static_cast<double>(d.e_query) : 0.0;
+          const double kt = t.K > 0.0 ? t.K : 1.0, kd = d.K > 0.0 ? d.K : 1.0;
+          rej = !(u * eq * kt < et * kd);
+          if (seg == 0 && P.p_draft) P.p_draft[static_cast<int64_t>(b) * G + i] = static_cast<float>(et / kt);
+          if (seg == 0 && P.q_draft) P.q_draft[static_cast<int64_t>(b) * G + i] = static_cast<float>(eq / kd);
+        }
+      }
+      const unsigned m = __ballot_sync(0xffffffffu, rej);
+      if (m && k == G) k = base + __ffs(m) - 1;
     }
-    if (st) atomicOr(&sh.status, st);
+    st = __reduce_or_sync(0xffffffffu, st);
+    // The draw's two rows: target k and (when k < γ) draft k.
+    if (lane == 0) sh.pt = draw_side(ts[k]);
+    if (lane == 1 && k < G) sh.pd = draw_side(ds[k]);
+    if (lane == 0) {
+      sh.k = k;
+      sh.status = st;
+    }
   }
   __syncthreads();
+  const unsigned status = sh.status;
   int32_t* out = P.out_tokens + static_cast<int64_t>(b) * (G + 1);
-  if (sh.status & (SV_ROW_BAD_DRAFT_ID | SV_ROW_EMPTY)) {
-    // Uniform over the cluster, before any distributed shared memory access.
-    if (rank == 0) {
+  if (status & (SV_ROW_BAD_DRAFT_ID | SV_ROW_EMPTY)) {
+    if (seg == 0) {
       for (int i = tid; i <= G; i += kDThreads) out[i] = -1;
       if (tid == 0) {
         if (P.num_accepted) P.num_accepted[b] = 0;
-        if (P.row_status) P.row_status[b] = static_cast<int32_t>(sh.status);
+        if (P.row_status) P.row_status[b] = static_cast<int32_t>(status);
         if (P.out_prob) P.out_prob[b] = 0.0f;
       }
     }
     return;
   }
-  if (tid == 0) {
-    int k = G;
-    for (int i = 0; i < G; ++i)
-      if (!sh.acc[i]) {
-        k = i;
-        break;
-      }
-    sh.k = k;
-  }
-  __syncthreads();
   const int k = sh.k;
-  const float u = P.u_resample ? P.u_resample[b] : 0.0f;
-  const RowStats& st = ts[k];
-  const ET* trow = reinterpret_cast<const ET*>(P.target) + (static_cast<int64_t>(b) * (G + 1) + k) * P.t_stride;
-  const ED* drow = k < G ? reinterpret_cast<const ED*>(P.draft) + (static_cast<int64_t>(b) * G + k) * P.d_stride
-                         : nullptr;
-  const DrawSide pt{st.mc, static_cast<float>(1.0 / st.K), st.tau, st.cut};
-  DrawSide pd{0.0f, 0.0f, 0u, 0};
-  if (k < G) pd = DrawSide{ds[k].mc, static_cast<float>(1.0 / ds[k].K), ds[k].tau, ds[k].cut};
-  const bool t_al = (reinterpret_cast<uintptr_t>(trow) & 15u) == 0;
-  const bool d_al = drow && (reinterpret_cast<uintptr_t>(drow) & 15u) == 0;
-  const int V = P.V;
-  const int nchunks = (V + kDChunk - 1) / kDChunk;
-  const int cpc = (nchunks + cld - 1) / cld;
-  const int c0 = min(nchunks, rank * cpc), c1 = min(nchunks, c0 + cpc);
-  const int warp = tid >> 5, lane = tid & 31;
-
   bool resid = k < G;
-  bool fallback = false;
-  double R = 0.0;
-  int last = -1;
-  for (int attempt = 0; attempt < 2; ++attempt) {
-    // Pass 1: chunk sums of this block's segment.
-    double seg = 0.0;
-    int lp = -1;
-    for (int ci = c0; ci < c1; ++ci) {
-      const int j0 = ci * kDChunk + tid * kDEPT;
-      float w[kDEPT];
-      weights8<ET, ED>(trow, drow, P.t2d, V, P.Vd, t_al, d_al, resid, P.c, pt, pd, j0, w);
-      float part = 0.0f;
+  const DrawSide pt = sh.pt;
+  const DrawSide pd = resid ? sh.pd : DrawSide{0.0f, 0.0f, 0u, 0};
+  RowView R;
+  R.trow = static_cast<const ET*>(P.target) + (static_cast<int64_t>(b) * (G + 1) + k) * P.t_stride;
+  R.drow = resid ? static_cast<const void*>(static_cast<const ED*>(P.draft) +
+                                            (static_cast<int64_t>(b) * G + k) * P.d_stride)
+                 : nullptr;
+  R.fast = (V % 8) == 0 && (reinterpret_cast<uintptr_t>(R.trow) & 15u) == 0 &&
+           (!resid || P.t2d || (reinterpret_cast<uintptr_t>(R.drow) & 15u) == 0);
+
+  // This block's chunks: per-chunk weight sums and the last positive id.
+  const int c0 = seg * NC;
+  float part[NC];
+  int lp = -1;
+  if (R.fast) {
+    segment_sums_fast<ET, ED, NC>(P, R, c0, resid, pt, pd, part, lp);
+  } else {
+#pragma unroll 1
+    for (int q = 0; q < NC; ++q) {
+      part[q] = 0.0f;
+      if (c0 + q >= nchunks) continue;
+      float w[8];
+      chunk_weights<ET, ED>(P, R, c0 + q, resid, pt, pd, w);
+      const int j0 = (c0 + q) * kDChunk + tid * kDEPT;
 #pragma unroll
-      for (int e = 0; e < kDEPT; ++e) {
-        part += w[e];
+      for (int e = 0; e < 8; ++e) {
+        part[q] += w[e];
         if (w[e] > 0.0f) lp = j0 + e;
       }
-      part = warp_sum(part);
-      if (lane == 0) sh.red[warp] = part;
-      __syncthreads();
-      if (warp == 0) {
-        float s = lane < kDThreads / 32 ? sh.red[lane] : 0.0f;
-        s = warp_sum(s);
-        if (lane == 0) {
-          chunk_sums[ci - c0] = s;
-          seg += static_cast<double>(s);
-        }
+    }
+  }
+#pragma unroll
+  for (int q = 0; q < NC; ++q) {
+    const float v = warp_sum(part[q]);
+    if (lane == 0) sh.wsum[q][warp] = v;
+  }
+  lp = warp_max_i(lp);
+  if (lane == 0) sh.red_i[warp] = lp;
+  __syncthreads();
+  float* csum = P.chunk_sums + static_cast<int64_t>(b) * nchunks;
+  int32_t* slast = P.seg_last + static_cast<int64_t>(b) * nseg;
+  if (tid < NC && c0 + tid < nchunks) {
+    float v = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kDWarps; ++w) v += sh.wsum[tid][w];
+    csum[c0 + tid] = v;
+  }
+  if (tid == 32) {
+    int l2 = -1;
+    for (int w = 0; w < kDWarps; ++w) l2 = max(l2, sh.red_i[w]);
+    slast[seg] = l2;
+  }
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) sh.last = atomicAdd(P.counters + b, 1u) == static_cast<unsigned>(nseg - 1);
+  __syncthreads();
+  if (!sh.last) return;
+  __threadfence();
+
+  // The row's last block: the total, and the chunk that holds u * total.
+  const float u = P.u_resample ? P.u_resample[b] : 0.0f;
+  bool fallback = false;
+  for (int attempt = 0; attempt < 2; ++attempt) {
+    if (warp == 0) {
+      const int per = (nchunks + 31) / 32;
+      const int q0 = min(nchunks, lane * per), q1 = min(nchunks, q0 + per);
+      double s = 0.0;
+      for (int q = q0; q < q1; ++q) s += static_cast<double>(__ldcg(csum + q));
+      double incl = s;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const double y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
       }
-      __syncthreads();
-    }
-    {
-      __shared__ int s_red_i[32];
-      lp = block_max_i<kDThreads>(lp, s_red_i);
-    }
-    if (tid == 0) {
-      sh.seg_total = seg;
-      sh.seg_last = lp;
+      const double total = __shfl_sync(0xffffffffu, incl, 31);
+      const double target = static_cast<double>(u) * total;
+      const unsigned hb = __ballot_sync(0xffffffffu, s > 0.0 && incl > target && incl - s <= target);
+      int lq = -1;
+      for (int sg = lane; sg < nseg; sg += 32) lq = max(lq, __ldcg(slast + sg));
+      lq = warp_max_i(lq);
+      int chunk = -1;
+      double carry = 0.0;
+      if (hb) {
+        const int wl = __ffs(hb) - 1;
+        if (lane == wl) {
+          double cc = incl - s;
+          for (int q = q0; q < q1; ++q) {
+            const double s2 = static_cast<double>(__ldcg(csum + q));
+            if (s2 > 0.0 && cc + s2 > target) {
+              chunk = q;
+              break;
+            }
+            cc += s2;
+          }
+          carry = cc;
+        }
+        chunk = __shfl_sync(0xffffffffu, chunk, wl);
+        carry = __shfl_sync(0xffffffffu, carry, wl);
+      }
+      if (lane == 0) {
+        sh.total = total;
+        sh.target = target;
+        sh.chunk = chunk;
+        sh.carry = carry;
+        sh.tok = lq;
+      }
     }
     __syncthreads();
-    cluster.sync();
-    R = 0.0;
-    last = -1;
-    for (int q = 0; q < cld; ++q) {
-      const DecideShared* p = cluster.map_shared_rank(&sh, q);
-      R += p->seg_total;
-      last = max(last, p->seg_last);
-    }
-    if (R > 0.0 || !resid) break;
-    // Residual mass 0 (possible only through rounding): draw from p_k.
+    if (sh.total > 0.0 || !resid) break;
+    // Residual mass 0 (possible only through rounding): draw from p_k.  This
+    // block recomputes the chunk sums of p_k by itself.
     resid = false;
     fallback = true;
-    cluster.sync();  // peers have read this block's totals
+    int lpf = -1;
+#pragma unroll 1
+    for (int ch = 0; ch < nchunks; ++ch) {
+      float w[8];
+      chunk_weights<ET, ED>(P, R, ch, false, pt, pd, w);
+      float s = 0.0f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        s += w[e];
+        if (w[e] > 0.0f) lpf = ch * kDChunk + tid * kDEPT + e;
+      }
+      s = block_sum_to0(s, sh);
+      if (tid == 0) csum[ch] = s;
+    }
+    lpf = block_max_i<kDThreads>(lpf, sh.red_i);
+    for (int sg = tid; sg < nseg; sg += kDThreads) slast[sg] = sg == 0 ? lpf : -1;
+    __syncthreads();
   }
-  if (tid == 0) {
-    sh.writer = 0;
-    sh.tok = last;
-    sh.chunk = -1;
-    if (R > 0.0) {
-      const double target = static_cast<double>(u) * R;
-      double cum = 0.0;
-      for (int q = 0; q < cld; ++q) {
-        const double tq = cluster.map_shared_rank(&sh, q)->seg_total;
-        if (cum + tq > target && tq > 0.0) {
-          sh.writer = q;
-          if (q == rank) {
-            // Find the chunk inside this block's segment.
-            double cc = cum;
-            for (int ci = c0; ci < c1; ++ci) {
-              const double s = chunk_sums[ci - c0];
-              if (cc + s > target && s > 0.0f) {
-                sh.chunk = ci;
-                sh.carry = cc;
-                break;
-              }
-              cc += s;
-            }
-          }
+  if (sh.total > 0.0 && sh.chunk >= 0) {
+    // Rescan the chunk that holds the draw: the thread whose ids span
+    // u * total (in block order) finds the id.
+    const int j0 = sh.chunk * kDChunk + tid * kDEPT;
+    float w[8];
+    chunk_weights<ET, ED>(P, R, sh.chunk, resid, pt, pd, w);
+    float mine = 0.0f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) mine += w[e];
+    double tot;
+    const double excl = block_exclusive_scan_d<kDThreads>(static_cast<double>(mine), sh.scan, &tot);
+    if (tid == 0) sh.best = INT32_MAX;
+    __syncthreads();
+    const double rem = sh.target - (sh.carry + excl);
+    if (rem < static_cast<double>(mine)) {
+      const float remf = static_cast<float>(rem);
+      float run = 0.0f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        run += w[e];
+        if (w[e] > 0.0f && run > remf) {
+          atomicMin(&sh.best, j0 + e);
           break;
         }
-        cum += tq;
-      }
-      sh.target = target;
-    }
-  }
-  __syncthreads();
-  if (sh.chunk >= 0) {
-    // Rescan the chunk that holds the draw.
-    const int j0 = sh.chunk * kDChunk + tid * kDEPT;
-    float w[kDEPT];
-    weights8<ET, ED>(trow, drow, P.t2d, V, P.Vd, t_al, d_al, resid, P.c, pt, pd, j0, w);
-    float part = 0.0f;
-    int lp = -1;
-#pragma unroll
-    for (int e = 0; e < kDEPT; ++e) {
-      part += w[e];
-      if (w[e] > 0.0f) lp = j0 + e;
-    }
-    double tot;
-    const double excl = block_exclusive_scan_d<kDThreads>(static_cast<double>(part), sh.scan, &tot);
-    __shared__ int s_best;
-    if (tid == 0) s_best = INT32_MAX;
-    __syncthreads();
-    double run = sh.carry + excl;
-#pragma unroll
-    for (int e = 0; e < kDEPT; ++e) {
-      run += w[e];
-      if (w[e] > 0.0f && run > sh.target) {
-        atomicMin(&s_best, j0 + e);
-        break;
       }
     }
-    __shared__ int s_red_i2[32];
-    lp = block_max_i<kDThreads>(lp, s_red_i2);
     __syncthreads();
-    if (tid == 0) sh.tok = s_best != INT32_MAX ? s_best : lp;
+    if (tid == 0 && sh.best != INT32_MAX) sh.tok = sh.best;
     __syncthreads();
   }
-  if (rank == sh.writer) {
-    const int tok = sh.tok;
-    for (int i = tid; i <= G; i += kDThreads)
-      out[i] = i < k ? P.ids[static_cast<int64_t>(b) * G + i] : (i == k ? tok : -1);
-    if (tid == 0) {
-      if (P.num_accepted) P.num_accepted[b] = k;
-      if (P.row_status)
-        P.row_status[b] = static_cast<int32_t>(sh.status | (fallback ? SV_ROW_RESAMPLE_FALLBACK : 0u));
-      if (P.out_prob) {
-        float pr = 0.0f;
-        if (!resid && tok >= 0) {
-          const float x = Elem<ET>::load(trow + tok);
-          if (kept(order_key(x), tok, pt.tau, pt.cut)) pr = weight(x, P.c, pt.mc) * pt.invK;
-        }
-        P.out_prob[b] = pr;
-      }
+  const int tok = sh.tok;
+  for (int i = tid; i <= G; i += kDThreads)
+    out[i] = i < k ? P.ids[static_cast<int64_t>(b) * G + i] : (i == k ? tok : -1);
+  if (tid == 0) {
+    if (P.num_accepted) P.num_accepted[b] = k;
+    if (P.row_status) P.row_status[b] = static_cast<int32_t>(status | (fallback ? SV_ROW_RESAMPLE_FALLBACK : 0u));
+    if (P.out_prob) {
+      float pr = 0.0f;
+      if (!resid && tok >= 0) pr = prob_of(Elem<ET>::load(static_cast<const ET*>(R.trow) + tok), tok, P.c, pt);
+      P.out_prob[b] = pr;
     }
   }
-  // No block may leave while a peer can still read its shared memory.
-  cluster.sync();
 }
 
-template <typename ET, typename ED>
-static sv_status launch_decide_typed(const DecideParams& P, cudaStream_t stream) {
+size_t decide_scratch_bytes(int B, int V) {
+  const size_t chunks = static_cast<size_t>(B) * static_cast<size_t>((V + kDChunk - 1) / kDChunk);
+  return align_up(chunks * sizeof(float), 256) + align_up(chunks * sizeof(int32_t), 256) +
+         align_up(static_cast<size_t>(B) * sizeof(unsigned), 256);
+}
+
+template <typename ET, typename ED, int NC>
+static sv_status launch_decide_typed(DecideParams P, void* scratch, cudaStream_t stream) {
   const int nchunks = (P.V + kDChunk - 1) / kDChunk;
-  const int cld = nchunks >= 8 ? 8 : (nchunks >= 4 ? 4 : (nchunks >= 2 ? 2 : 1));
-  const int cpc = (nchunks + cld - 1) / cld;
-  const size_t smem = align_up(static_cast<size_t>(cpc) * sizeof(float), 16);
-  auto kern = decide_kernel<ET, ED>;
-  static FuncAttrCache cache;
-  if (smem > 48 * 1024 && !cache.ensure(reinterpret_cast<const void*>(kern), smem, false)) return SV_ERR_CUDA;
-  cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(static_cast<unsigned>(P.B) * cld);
-  cfg.blockDim = dim3(kDThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = static_cast<unsigned>(cld);
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, kern, P, cld) != cudaSuccess) return SV_ERR_CUDA;
+  const int nseg = (nchunks + NC - 1) / NC;
+  const size_t chunks = static_cast<size_t>(P.B) * nchunks;
+  char* s = static_cast<char*>(scratch);
+  P.chunk_sums = reinterpret_cast<float*>(s);
+  P.seg_last = reinterpret_cast<int32_t*>(s + align_up(chunks * sizeof(float), 256));
+  P.counters = reinterpret_cast<unsigned*>(s + align_up(chunks * sizeof(float), 256) +
+                                           align_up(chunks * sizeof(int32_t), 256));
+  const size_t blocks = static_cast<size_t>(P.B) * nseg;
+  if (blocks > INT32_MAX) return SV_ERR_UNSUPPORTED;
+  if (cudaMemsetAsync(P.counters, 0, static_cast<size_t>(P.B) * sizeof(unsigned), stream) != cudaSuccess)
+    return SV_ERR_CUDA;
+  decide_kernel<ET, ED, NC><<<static_cast<unsigned>(blocks), kDThreads, 0, stream>>>(P, nseg);
+  if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
   note_launch(stream);
   return SV_OK;
 }
 
-sv_status launch_decide(const DecideParams& P, sv_dtype td, sv_dtype dd, cudaStream_t stream) {
+sv_status launch_decide(const DecideParams& P, sv_dtype td, sv_dtype dd, void* scratch, cudaStream_t stream) {
   if (P.B == 0) return SV_OK;
   const bool tb = td == SV_BF16, db = dd == SV_BF16;
-  if (tb && db) return launch_decide_typed<uint16_t, uint16_t>(P, stream);
-  if (tb) return launch_decide_typed<uint16_t, float>(P, stream);
-  if (db) return launch_decide_typed<float, uint16_t>(P, stream);
-  return launch_decide_typed<float, float>(P, stream);
+  if (tb && db && !P.t2d) return launch_decide_typed<uint16_t, uint16_t, 8>(P, scratch, stream);
+  if (tb && db) return launch_decide_typed<uint16_t, uint16_t, 4>(P, scratch, stream);
+  if (tb) return launch_decide_typed<uint16_t, float, 4>(P, scratch, stream);
+  if (db) return launch_decide_typed<float, uint16_t, 4>(P, scratch, stream);
+  return launch_decide_typed<float, float, 4>(P, scratch, stream);
 }
 
 }  // namespace sv

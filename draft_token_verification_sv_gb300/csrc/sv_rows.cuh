@@ -87,9 +87,16 @@ struct DecideParams {
   float* q_draft;
   int32_t* row_status;
   float* out_prob;
+  // Scratch, set by launch_decide: per-chunk draw-weight sums, the last id
+  // with a positive weight per block, finished blocks per row.
+  float* chunk_sums;
+  int32_t* seg_last;
+  unsigned* counters;
 };
 
-sv_status launch_decide(const DecideParams& P, sv_dtype target_dtype, sv_dtype draft_dtype, cudaStream_t stream);
+// The decision/draw pass with `scratch` of decide_scratch_bytes(B, V) bytes.
+sv_status launch_decide(const DecideParams& P, sv_dtype target_dtype, sv_dtype draft_dtype, void* scratch,
+                        cudaStream_t stream);
 
 // Top-p statistics of every row of L (sv_topp.cu), with `scratch` of
 // topp_scratch_bytes(...) bytes (slice summaries and row counters).

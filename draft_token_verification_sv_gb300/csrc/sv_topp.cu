@@ -97,7 +97,7 @@ __device__ __forceinline__ void for_row(const E* row, int len, F&& f) {
   constexpr int EPV = Elem<E>::kPerVec;
   const RowSplit rs = split_row(row, len);
   const uint4* vp = reinterpret_cast<const uint4*>(row + rs.head);
-  constexpr int U = 8;
+  constexpr int U = 4;
   // Block-uniform trip count: f may use full-warp votes.
   for (int base = 0; base < rs.nvec; base += kSThreads * U) {
     const int v0 = base + static_cast<int>(threadIdx.x);
@@ -590,11 +590,13 @@ __global__ void __launch_bounds__(kSThreads, 2) topp_slice_kernel(StatsLaunch L)
   // 1. The slice in registers; slice maximum.
   const RowSplit rs = split_row(row, S.len);
   const uint4* vp = reinterpret_cast<const uint4*>(row + rs.head);
+  // Normal L2 policy (not the streaming evict-first one): the row's last
+  // block rescans this slice from L2.
   uint4 raw[VPT];
 #pragma unroll
   for (int k = 0; k < VPT; ++k) {
     const int v = s * VPS + k * kSThreads + tid;
-    raw[k] = v < rs.nvec ? ldg_stream(vp + v) : Elem<E>::neg_inf_vec();
+    raw[k] = v < rs.nvec ? __ldcg(vp + v) : Elem<E>::neg_inf_vec();
   }
   float xv = -CUDART_INF_F;
   if (s == 0) {
