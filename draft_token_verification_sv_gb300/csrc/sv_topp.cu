@@ -9,21 +9,25 @@
 //
 // Work split, without clusters and without any block waiting for another:
 //  * slice blocks: every block reads one slice of 8192 logits of a row into
-//    registers, takes the slice maximum m_s, and adds e_s = 2^(l*c - m_s*c)
-//    (c = log2(e)/T) to a per-thread private histogram keyed by the ABSOLUTE
-//    half-octave g = floor(2*l*c) of the logit ([bin][thread] layout, no
-//    atomics).  It publishes (m_s, bins, mass below the bins) and bumps the
-//    row's counter;
-//  * the row's last slice block merges the summaries (absolute bins line up
-//    across slices after scaling by 2^((m_s - m)*c)), finds the half-octave
-//    g* where the cumulative mass from the top first exceeds top_p * S, then
-//    rescans the row (just read by its sibling blocks, so served by L2) for
-//    the logits of g*, refines them on finer sub-bins of 2*l*c in shared
-//    memory, and resolves the last <= 64 exactly: sorted by (logit
-//    descending, tie key ascending), walked in double precision.
-// Rare rows (the cut below the 64 half-octaves under the maximum, more than
-// 16384 candidates, or a large group of different logits that 2*l*c cannot
-// separate) take an exact radix select over the order keys of the row.
+//    registers and takes the slice maximum.  Each logit falls in the
+//    ABSOLUTE eighth-octave bin f = floor(8 * l * c) (c = log2(e)/T), so that
+//    bins line up across the slices of a row.  The 256 bins below the slice
+//    maximum collect the logits' masses in fixed point relative to the bin's
+//    upper edge, v = round(2^21 * 2^(l*c - (f+1)/8)), summed exactly in
+//    per-warp u32 histograms (shared-memory integer reductions, no read-
+//    modify-write chains); lower logits add 2^(l*c - m_s*c) to a "far" sum.
+//    The block publishes (m_s, far, top bin, 256 bin sums) and bumps the row's
+//    counter;
+//  * the row's last slice block merges the summaries (a bin's mass is its
+//    summed v times 2^((f+1)/8 - 21 - m*c) whichever slice it came from),
+//    finds the bin f* where the mass from the top first exceeds top_p * S,
+//    rescans the row (just read by its sibling blocks, so served by L2) to
+//    collect the logits of f* with their ids in shared memory, and resolves
+//    the cut among them by radix levels over their order keys, ending with
+//    an exact sort of the last <= 64 by (logit descending, tie key ascending)
+//    walked in double precision.
+// Rare rows (the cut below the 32 octaves under the maximum, more than 4096
+// logits in f*) take an exact radix select over the order keys of the row.
 #include "sv_rows.cuh"
 
 namespace sv {
@@ -31,30 +35,36 @@ namespace sv {
 constexpr int kSThreads = 256;
 constexpr int kSEPT = 32;                       // logits per thread per slice
 constexpr int kSlice = kSThreads * kSEPT;       // logits per slice
-constexpr int kGB = 64;                         // half-octave bins below the maximum
-constexpr int kSummary = 4 + kGB;               // floats per slice summary
-constexpr int kListCap = 16384;                 // candidate indices in shared memory
+constexpr int kNB = 256;                        // eighth-octave bins under a slice maximum
+constexpr int kSummary = 4 + kNB;               // floats per slice summary
+constexpr int kCandCap = 4096;                  // candidates of the cut bin in shared memory
 constexpr int kFinal = 64;
 constexpr int kWarps = kSThreads / 32;
+constexpr float kFixBin = 2097152.0f;           // 2^21: slice bin masses, units of the bin's upper edge
+constexpr float kFixCand = 524288.0f;           // 2^19: candidate level masses
 constexpr double kScale40 = 1099511627776.0;    // generic path: masses in units of 2^-40
 constexpr double kInv40 = 1.0 / 1099511627776.0;
 
 struct ToppShared {
   union {
-    float phist[kGB * kSThreads];               // slice phase: private bin masses
-    int list[kListCap];                         // merge phase: candidate indices
+    unsigned wh[kWarps][kNB];                   // slice phase: per-warp bin sums (fixed point)
+    struct {
+      float x[kCandCap];                        // merge phase: candidate logits
+      int j[kCandCap];                          //              and their ids
+    } cand;
+    unsigned gh[4][256];                        // generic path: count and 3 mass limbs
   };
-  unsigned wl[kWarps][3][256];                  // per-warp level histograms (count, lo, hi)
+  unsigned hcnt[256];
+  unsigned hmass[256];
   unsigned long long tmass[256];
   unsigned tcnt[256];
-  float mbins[kWarps][kGB];
-  float mfar[kWarps];
+  double scan[32];
   float red_f[32];
   unsigned long long red_u[32];
   int gidx[kFinal];
   int wcnt[kWarps];
   int last;
-  int cn;
+  int ncand;
   int sel;
   int found;
   unsigned long long sel_above;
@@ -62,7 +72,7 @@ struct ToppShared {
   int gstar;
   int pick_sec;
   unsigned pick_key;
-  double above0, limit, total, kept_mass;
+  double above0, limit, total, kept_mass, unit;
 };
 
 // exp2 that the compiler may not merge with an identical earlier one.
@@ -71,10 +81,6 @@ __device__ __forceinline__ float ex2v(float x) {
   asm volatile("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
-
-// Absolute half-octave of a logit: floor(2 * l * c).  The same expression
-// everywhere, so membership is decided identically in every pass.
-__device__ __forceinline__ int half_octave(float l, float c) { return __float2int_rd(2.0f * (l * c)); }
 
 template <typename E>
 __device__ __forceinline__ float widen(const uint4& v, int i) {
@@ -90,6 +96,20 @@ __device__ __forceinline__ float widen(const uint4& v, int i) {
   }
 }
 
+// 2^n for an integer n in the normal double range.
+__device__ __forceinline__ double pow2i(int n) {
+  return __longlong_as_double(static_cast<long long>(n + 1023) << 52);
+}
+
+// 2^(i/8) for i = 0..7, from the binary digits of i.
+__device__ __forceinline__ double pow2_eighths(int i) {
+  double r = 1.0;
+  if (i & 1) r *= 1.0905077326652577;  // 2^(1/8)
+  if (i & 2) r *= 1.1892071150027210;  // 2^(1/4)
+  if (i & 4) r *= 1.4142135623730951;  // 2^(1/2)
+  return r;
+}
+
 // Visit every logit of a row (body vectors strided over the block, then the
 // scalar head and tail): f(value, index), index -1 for padding.
 template <typename E, typename F>
@@ -97,7 +117,7 @@ __device__ __forceinline__ void for_row(const E* row, int len, F&& f) {
   constexpr int EPV = Elem<E>::kPerVec;
   const RowSplit rs = split_row(row, len);
   const uint4* vp = reinterpret_cast<const uint4*>(row + rs.head);
-  constexpr int U = 4;
+  constexpr int U = 8;
   // Block-uniform trip count: f may use full-warp votes.
   for (int base = 0; base < rs.nvec; base += kSThreads * U) {
     const int v0 = base + static_cast<int>(threadIdx.x);
@@ -215,27 +235,6 @@ __device__ __forceinline__ void crossing_count(ToppShared& sh, unsigned need) {
   }
 }
 
-__device__ __forceinline__ void clear_wl(ToppShared& sh) {
-  unsigned* w = &sh.wl[0][0][0];
-  for (int t = threadIdx.x; t < kWarps * 3 * 256; t += kSThreads) w[t] = 0u;
-}
-
-// Merge the per-warp level histograms into sh.tmass / sh.tcnt.
-__device__ __forceinline__ void merge_wl(ToppShared& sh) {
-  for (int t = threadIdx.x; t < 256; t += kSThreads) {
-    unsigned long long lo = 0, hi = 0;
-    unsigned cnt = 0;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-      cnt += sh.wl[w][0][t];
-      lo += sh.wl[w][1][t];
-      hi += sh.wl[w][2][t];
-    }
-    sh.tcnt[t] = cnt;
-    sh.tmass[t] = lo + (hi << 16);
-  }
-}
-
 template <typename E>
 __device__ __forceinline__ float load_at(const E* row, int j) {
   if constexpr (sizeof(E) == 4) return __ldcg(reinterpret_cast<const float*>(row) + j);
@@ -249,7 +248,7 @@ template <typename E>
 __device__ __noinline__ void generic_select(ToppShared& sh, const E* row, const RowSet& S, float c, float mc,
                                             float top_p, uint32_t& tau_out, int32_t& cut_out, double& K_out) {
   constexpr int kPasses = sizeof(E) == 2 ? 2 : 4;
-  unsigned* h = &sh.wl[0][0][0];  // [count, m0, m1, m2][256]
+  unsigned* h = &sh.gh[0][0];  // [count, m0, m1, m2][256]
   uint32_t prefix = 0;
   unsigned long long above = 0, limit = 0, total = 0, grp_mass = 0;
   unsigned grp_cnt = 0;
@@ -345,140 +344,103 @@ __device__ __noinline__ void generic_select(ToppShared& sh, const E* row, const 
   K_out = static_cast<double>(above + nk * e_tau) * kInv40;
 }
 
-// The row's cut from the merged half-octave bins (last slice block only).
-// Returns false when the row needs the generic path.
+// The cut among the candidates of the cut bin (n <= kCandCap, in
+// sh.cand): radix levels over their order keys, each keeping the digit where
+// the mass from the top first exceeds the limit (counts and fixed-point
+// masses v = round(2^19 * 2^(l*c + nb)), nb = -(f*+1)/8), then an exact sort
+// of the last <= 64 walked in double precision, or for a larger group of
+// equal logits a cut by tie key.  above0 and limit are masses relative to the
+// row maximum; `unit` is the mass of one fixed-point unit.
 template <typename E>
-__device__ bool resolve_row(ToppShared& sh, const E* row, const RowSet& S, float c, float mc, int gstar,
-                            double above0, double limit, uint32_t& tau, int32_t& cut, double& K) {
+__device__ void resolve_candidates(ToppShared& sh, const RowSet& S, float c, float mc, int n, float nb,
+                                   double above0, double limit, double unit, uint32_t& tau, int32_t& cut,
+                                   double& K) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const unsigned lane_lt = (1u << lane) - 1u;
-  // Masses of the cut half-octave: e < 2^((g*+1)/2 - mc) <= 2^k, held as
-  // e * 2^(30 - k) < 2^30 in fixed point.
-  const int k = static_cast<int>(ceilf(0.5f * static_cast<float>(gstar + 1) - mc)) + 1;
-  const float lscale = ldexpf(1.0f, 30 - k);
-  const float g_lo = static_cast<float>(gstar);
-  constexpr int kRegion = kListCap / kWarps;
-  // Rescan: candidates of g*, level-1 histogram on floor(256 * (2lc - g*)).
-  clear_wl(sh);
-  __syncthreads();
-  int wbase = 0;
-  for_row<E>(row, S.len, [&](float x, int j) {
-    const bool cand = j >= 0 && half_octave(x, c) == gstar;
-    const unsigned bal = __ballot_sync(0xffffffffu, cand);
-    if (cand) {
-      const float u = 2.0f * (x * c) - g_lo;
-      const int s1 = min(255, max(0, static_cast<int>(u * 256.0f)));
-      const unsigned v = __float2uint_rn(ex2v(fmaf(x, c, -mc)) * lscale);
-      atomicAdd(&sh.wl[warp][0][s1], 1u);
-      atomicAdd(&sh.wl[warp][1][s1], v & 0xffffu);
-      atomicAdd(&sh.wl[warp][2][s1], v >> 16);
-      const int slot = wbase + __popc(bal & lane_lt);
-      if (slot < kRegion) sh.list[warp * kRegion + slot] = j;
-    }
-    wbase += __popc(bal);
-  });
-  if (lane == 0) sh.wcnt[warp] = wbase;
-  __syncthreads();
-  merge_wl(sh);
-  int over = 0, cn = 0, my_off = 0;
-#pragma unroll
-  for (int w = 0; w < kWarps; ++w) {
-    const int n = sh.wcnt[w];
-    over |= n > kRegion;
-    if (w < warp) my_off += n;
-    cn += n;
+  uint32_t kmin = 0xffffffffu, kmax = 0u;
+  for (int i = tid; i < n; i += kSThreads) {
+    const uint32_t k = order_key(sh.cand.x[i]);
+    kmin = min(kmin, k);
+    kmax = max(kmax, k);
   }
-  if (over) return false;  // uniform: every thread read the same counts
-  // Pack the warp regions into the front of the list, in warp order (a
-  // warp's destination never overlaps a later warp's region).
-  for (int w = 1; w < kWarps; ++w) {
-    __syncthreads();
-    if (warp == w) {
-      const int n = sh.wcnt[w];
-      for (int e2 = lane; e2 < n; e2 += 32) sh.list[my_off + e2] = sh.list[w * kRegion + e2];
+  kmax = static_cast<uint32_t>(block_max_u64<kSThreads>(kmax, sh.red_u));
+  kmin = 0xffffffffu - static_cast<uint32_t>(block_max_u64<kSThreads>(0xffffffffu - kmin, sh.red_u));
+  const double lim_rel = limit - above0;
+  const unsigned long long lim_f = lim_rel > 0.0 ? static_cast<unsigned long long>(lim_rel / unit) : 0ull;
+  unsigned long long above_f = 0;
+  uint32_t kbase = kmin;
+  const uint32_t span = kmax - kmin;
+  int shift = span ? max(0, 32 - __clz(static_cast<int>(span)) - 8) : 0;
+  int cnt = n;
+#pragma unroll 1
+  for (;;) {
+    for (int t = tid; t < 256; t += kSThreads) {
+      sh.hcnt[t] = 0u;
+      sh.hmass[t] = 0u;
     }
-  }
-  __syncthreads();
-  const unsigned long long lim_fixed =
-      limit > above0 ? static_cast<unsigned long long>((limit - above0) * static_cast<double>(lscale)) : 0ull;
-  unsigned long long above_fixed = 0;
-  // Levels: sub-bin floor(256^(L+1) * (2lc - g*)) with the earlier digits fixed.
-  int pref = 0;
-  for (int lvl = 0;; ++lvl) {
-    crossing_desc(sh, 255, above_fixed, lim_fixed);
     __syncthreads();
-    const int sel = sh.sel;
-    above_fixed = sh.sel_above;
-    const unsigned grp = sh.sel_cnt;
-    pref = pref * 256 + sel;
-    const float scale_l = lvl == 0 ? 256.0f : (lvl == 1 ? 65536.0f : 16777216.0f);
+    for (int i = tid; i < cnt; i += kSThreads) {
+      const float x = sh.cand.x[i];
+      const uint32_t d = (order_key(x) - kbase) >> shift;
+      atomicAdd(&sh.hcnt[d], 1u);
+      atomicAdd(&sh.hmass[d], __float2uint_rn(ex2v(fmaf(x, c, nb)) * kFixCand));
+    }
     __syncthreads();
-    {
-      // Keep only the chosen sub-bin, order preserved: chunks of one entry
-      // per thread, block-wide scan of the keep flags, in-place writes (a
-      // chunk is read completely before any of it is written).
-      int kept_n = 0;
-      for (int b0 = 0; b0 < cn; b0 += kSThreads) {
-        const int s = b0 + tid;
-        bool keep = false;
-        int jv = 0;
-        if (s < cn) {
-          jv = sh.list[s];
-          const float u = 2.0f * (load_at<E>(row, jv) * c) - g_lo;
-          keep = static_cast<int>(u * scale_l) == pref;
-        }
-        const unsigned bal = __ballot_sync(0xffffffffu, keep);
-        if (lane == 0) sh.wcnt[warp] = __popc(bal);
-        __syncthreads();
-        int off = kept_n, chunk = 0;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) {
-          const int n = sh.wcnt[w];
-          if (w < warp) off += n;
-          chunk += n;
-        }
-        if (keep) sh.list[off + __popc(bal & lane_lt)] = jv;
-        kept_n += chunk;
-        __syncthreads();
+    for (int t = tid; t < 256; t += kSThreads) {
+      sh.tcnt[t] = sh.hcnt[t];
+      sh.tmass[t] = sh.hmass[t];
+    }
+    __syncthreads();
+    crossing_desc(sh, 255, above_f, lim_f);
+    __syncthreads();
+    const uint32_t dsel = static_cast<uint32_t>(sh.sel);
+    above_f = sh.sel_above;
+    // Keep the candidates of digit dsel, in order, in place: chunks of one
+    // entry per thread, each read completely before any of it is written.
+    int kept_n = 0;
+    for (int b0 = 0; b0 < cnt; b0 += kSThreads) {
+      const int i = b0 + tid;
+      bool keep = false;
+      float xv = 0.0f;
+      int jv = 0;
+      if (i < cnt) {
+        xv = sh.cand.x[i];
+        jv = sh.cand.j[i];
+        keep = ((order_key(xv) - kbase) >> shift) == dsel;
       }
-      if (tid == 0) sh.cn = kept_n;
+      const unsigned bal = __ballot_sync(0xffffffffu, keep);
+      if (lane == 0) sh.wcnt[warp] = __popc(bal);
+      __syncthreads();
+      int off = kept_n, chunk = 0;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        const int nw = sh.wcnt[w];
+        if (w < warp) off += nw;
+        chunk += nw;
+      }
+      if (keep) {
+        sh.cand.x[off + __popc(bal & lane_lt)] = xv;
+        sh.cand.j[off + __popc(bal & lane_lt)] = jv;
+      }
+      kept_n += chunk;
+      __syncthreads();
     }
-    __syncthreads();
-    cn = sh.cn;
-    if (grp <= static_cast<unsigned>(kFinal) || lvl == 2) break;
-    const float scale_n = lvl == 0 ? 65536.0f : 16777216.0f;
-    clear_wl(sh);
-    __syncthreads();
-    for (int s = tid; s < cn; s += kSThreads) {
-      const int jv = sh.list[s];
-      const float x = load_at<E>(row, jv);
-      const float u = 2.0f * (x * c) - g_lo;
-      const int sb = min(255, max(0, static_cast<int>(u * scale_n) - pref * 256));
-      const unsigned v = __float2uint_rn(ex2v(fmaf(x, c, -mc)) * lscale);
-      atomicAdd(&sh.wl[warp][0][sb], 1u);
-      atomicAdd(&sh.wl[warp][1][sb], v & 0xffffu);
-      atomicAdd(&sh.wl[warp][2][sb], v >> 16);
-    }
-    __syncthreads();
-    merge_wl(sh);
-    __syncthreads();
+    cnt = kept_n;
+    kbase += dsel << shift;
+    if (cnt <= kFinal || shift == 0) break;
+    shift = max(0, shift - 8);
   }
-  const double above = above0 + static_cast<double>(above_fixed) / static_cast<double>(lscale);
-  if (cn <= kFinal) {
+  const double above = above0 + static_cast<double>(above_f) * unit;
+  if (cnt <= kFinal) {
     // Sort the final group by (logit descending, tie key ascending), walk it.
     if (warp == 0) {
       unsigned long long a = 0, b = 0;
-      int ja = -1, jb = -1;
-      if (lane < cn) {
-        ja = sh.list[lane];
-        a = (static_cast<unsigned long long>(order_key(load_at<E>(row, ja))) << 32) |
-            (0xffffffffu - static_cast<uint32_t>(tie_key(S, ja)));
-      }
-      if (lane + 32 < cn) {
-        jb = sh.list[lane + 32];
-        b = (static_cast<unsigned long long>(order_key(load_at<E>(row, jb))) << 32) |
-            (0xffffffffu - static_cast<uint32_t>(tie_key(S, jb)));
-      }
+      if (lane < cnt)
+        a = (static_cast<unsigned long long>(order_key(sh.cand.x[lane])) << 32) |
+            (0xffffffffu - static_cast<uint32_t>(tie_key(S, sh.cand.j[lane])));
+      if (lane + 32 < cnt)
+        b = (static_cast<unsigned long long>(order_key(sh.cand.x[lane + 32])) << 32) |
+            (0xffffffffu - static_cast<uint32_t>(tie_key(S, sh.cand.j[lane + 32])));
       int ra = 0, rb = 0;
 #pragma unroll 4
       for (int j2 = 0; j2 < 32; ++j2) {
@@ -487,26 +449,25 @@ __device__ bool resolve_row(ToppShared& sh, const E* row, const RowSet& S, float
         ra += (xa2 > a) + (xb2 > a);
         rb += (xa2 > b) + (xb2 > b);
       }
-      if (lane < cn) sh.gidx[ra] = ja;
-      if (lane + 32 < cn) sh.gidx[rb] = jb;
+      if (lane < cnt) sh.gidx[ra] = lane;
+      if (lane + 32 < cnt) sh.gidx[rb] = lane + 32;
       __syncwarp();
       if (lane == 0) {
         double cum = above;
-        int pick = cn - 1;
-        for (int j2 = 0; j2 < cn; ++j2) {
-          const double e = static_cast<double>(weight(load_at<E>(row, sh.gidx[j2]), c, mc));
+        int pick = cnt - 1;
+        for (int r = 0; r < cnt; ++r) {
+          const double e = static_cast<double>(weight(sh.cand.x[sh.gidx[r]], c, mc));
           if (cum + e > limit) {
-            pick = j2;
+            pick = r;
             break;
           }
           cum += e;
         }
         double kept_mass = above;
-        for (int j2 = 0; j2 <= pick; ++j2)
-          kept_mass += static_cast<double>(weight(load_at<E>(row, sh.gidx[j2]), c, mc));
-        const int jp = sh.gidx[pick];
-        sh.pick_key = order_key(load_at<E>(row, jp));
-        sh.pick_sec = tie_key(S, jp);
+        for (int r = 0; r <= pick; ++r) kept_mass += static_cast<double>(weight(sh.cand.x[sh.gidx[r]], c, mc));
+        const int ip = sh.gidx[pick];
+        sh.pick_key = order_key(sh.cand.x[ip]);
+        sh.pick_sec = tie_key(S, sh.cand.j[ip]);
         sh.kept_mass = kept_mass;
       }
     }
@@ -514,43 +475,30 @@ __device__ bool resolve_row(ToppShared& sh, const E* row, const RowSet& S, float
     tau = sh.pick_key;
     cut = sh.pick_sec;
     K = sh.kept_mass;
-    return true;
+    return;
   }
-  // A group that 2*l*c cannot split: equal logits are cut by tie key;
-  // different logits go to the exact generic path.
-  uint32_t kmin = 0xffffffffu, kmax = 0u;
-  for (int s = tid; s < cn; s += kSThreads) {
-    const uint32_t key = order_key(load_at<E>(row, sh.list[s]));
-    kmin = min(kmin, key);
-    kmax = max(kmax, key);
-  }
-  kmax = static_cast<uint32_t>(block_max_u64<kSThreads>(kmax, sh.red_u));
-  kmin = static_cast<uint32_t>(~block_max_u64<kSThreads>(~static_cast<unsigned long long>(kmin) & 0xffffffffull,
-                                                          sh.red_u) & 0xffffffffull);
-  if (kmin != kmax) return false;
-  const float xv = __uint_as_float(kmin & 0x80000000u ? (kmin & 0x7fffffffu) : ~kmin);
-  const double e_g = static_cast<double>(weight(xv, c, mc));
+  // More than 64 equal logits at the cut: keep the nk with the lowest tie keys.
+  const double e_g = static_cast<double>(weight(sh.cand.x[0], c, mc));
   double nkd = floor((limit - above) / e_g) + 1.0;
   if (!(nkd >= 1.0)) nkd = 1.0;
-  const unsigned nk = nkd >= static_cast<double>(cn) ? static_cast<unsigned>(cn) : static_cast<unsigned>(nkd);
-  tau = kmin;
+  const unsigned nk = nkd >= static_cast<double>(cnt) ? static_cast<unsigned>(cnt) : static_cast<unsigned>(nkd);
+  tau = kbase;
   K = above + static_cast<double>(nk) * e_g;
   cut = INT32_MAX;
-  if (nk < static_cast<unsigned>(cn)) {
-    unsigned* h = &sh.wl[0][0][0];
+  if (nk < static_cast<unsigned>(cnt)) {
     uint32_t sp = 0;
     unsigned need = nk;
 #pragma unroll 1
     for (int q = 0; q < 3; ++q) {
       const int sb = 16 - 8 * q;
-      for (int t = tid; t < 256; t += kSThreads) h[t] = 0u;
+      for (int t = tid; t < 256; t += kSThreads) sh.hcnt[t] = 0u;
       __syncthreads();
-      for (int s = tid; s < cn; s += kSThreads) {
-        const uint32_t s2 = static_cast<uint32_t>(tie_key(S, sh.list[s]));
-        if (q == 0 || (s2 >> (sb + 8)) == sp) atomicAdd(&h[(s2 >> sb) & 255], 1u);
+      for (int s = tid; s < cnt; s += kSThreads) {
+        const uint32_t s2 = static_cast<uint32_t>(tie_key(S, sh.cand.j[s]));
+        if (q == 0 || (s2 >> (sb + 8)) == sp) atomicAdd(&sh.hcnt[(s2 >> sb) & 255], 1u);
       }
       __syncthreads();
-      for (int t = tid; t < 256; t += kSThreads) sh.tcnt[t] = h[t];
+      for (int t = tid; t < 256; t += kSThreads) sh.tcnt[t] = sh.hcnt[t];
       __syncthreads();
       crossing_count(sh, need);
       __syncthreads();
@@ -560,11 +508,10 @@ __device__ bool resolve_row(ToppShared& sh, const E* row, const RowSet& S, float
     }
     cut = static_cast<int32_t>(sp);
   }
-  return true;
 }
 
 template <typename E>
-__global__ void __launch_bounds__(kSThreads, 2) topp_slice_kernel(StatsLaunch L) {
+__global__ void __launch_bounds__(kSThreads, 3) topp_slice_kernel(StatsLaunch L) {
   constexpr int EPV = Elem<E>::kPerVec;
   constexpr int VPT = kSEPT / EPV;          // 16-byte vectors per thread
   constexpr int VPS = VPT * kSThreads;      // vectors per slice
@@ -586,12 +533,16 @@ __global__ void __launch_bounds__(kSThreads, 2) topp_slice_kernel(StatsLaunch L)
   const int sbase = (set ? L.set[0].rows * L.nslices[0] : 0) + r * ns;
   const E* row = reinterpret_cast<const E*>(S.base) + static_cast<int64_t>(r) * S.stride;
   const float c = L.c;
+  const float c8 = c * 8.0f;  // 8 * (l * c) == l * c8 exactly
 
-  // 1. The slice in registers; slice maximum.
+  // Per-warp bin sums start at zero (visible after the barriers of block_max).
+#pragma unroll
+  for (int i = 0; i < kWarps * kNB / kSThreads; ++i) (&sh.wh[0][0])[i * kSThreads + tid] = 0u;
+
+  // 1. The slice in registers; slice maximum.  Normal L2 policy (not the
+  // streaming evict-first one): the row's last block rescans it from L2.
   const RowSplit rs = split_row(row, S.len);
   const uint4* vp = reinterpret_cast<const uint4*>(row + rs.head);
-  // Normal L2 policy (not the streaming evict-first one): the row's last
-  // block rescans this slice from L2.
   uint4 raw[VPT];
 #pragma unroll
   for (int k = 0; k < VPT; ++k) {
@@ -613,19 +564,23 @@ __global__ void __launch_bounds__(kSThreads, 2) topp_slice_kernel(StatsLaunch L)
     for (int i = 0; i < EPV; ++i) lm = fmaxf(lm, Elem<E>::at(raw[k], i));
   const float ms = block_max<kSThreads>(lm, sh.red_f);
 
-  // 2. e relative to the slice maximum, binned by absolute half-octave.
-  float* ph = sh.phist;
-#pragma unroll 8
-  for (int b = 0; b < kGB; ++b) ph[b * kSThreads + tid] = 0.0f;
+  // 2. Bin sums over the 256 eighth-octaves under the slice maximum; the
+  // rest adds 2^(l*c - m_s*c) to `far`.
   const bool live = ms > -CUDART_INF_F;
-  const int Gs = live ? half_octave(ms, c) : 0;
+  const float Gsf = live ? floorf(ms * c8) : 0.0f;
+  const float lowf = Gsf - static_cast<float>(kNB);
   const float mcs = ms * c;
   float far = 0.0f;
+  unsigned* wh = sh.wh[warp];
   auto add = [&](float x) {
-    const float e = ex2(fmaf(x, c, -mcs));
-    const int loc = Gs - half_octave(x, c);
-    if (loc >= 0 && loc < kGB) ph[loc * kSThreads + tid] += e;
-    else far += e;
+    const float fy = floorf(x * c8);
+    if (fy > lowf) {
+      // l*c - (f+1)/8 in [-1/8, 0]: the mass relative to the bin's upper edge.
+      const float t = fmaf(x, c, fmaf(fy, -0.125f, -0.125f));
+      atomicAdd(&wh[static_cast<int>(Gsf - fy)], __float2uint_rn(ex2v(t) * kFixBin));
+    } else {
+      far += ex2v(fmaf(x, c, -mcs));
+    }
   };
   if (live) {
 #pragma unroll
@@ -635,34 +590,33 @@ __global__ void __launch_bounds__(kSThreads, 2) topp_slice_kernel(StatsLaunch L)
     if (xv > -CUDART_INF_F) add(xv);
   }
   __syncthreads();
-  // Slice totals per bin: 4 threads per bin, 64 columns each (rotated so the
-  // lanes of a warp hit different banks).
+  // Publish: slot t holds bin Gs - t.
   float* out = L.summ + static_cast<int64_t>(sbase + s) * kSummary;
   {
-    const int b = tid >> 2, part = tid & 3;
-    float acc = 0.0f;
-#pragma unroll 8
-    for (int t = 0; t < 64; ++t) acc += ph[b * kSThreads + part * 64 + ((t + 4 * (b & 7) + part) & 63)];
-    acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-    acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-    if (part == 0) out[4 + b] = acc;
+    unsigned long long a = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) a += sh.wh[w][tid];
+    out[4 + tid] = static_cast<float>(a);
   }
   far = block_sum<kSThreads>(far, sh.red_f);
   if (tid == 0) {
     out[0] = ms;
     out[1] = far;
-    __threadfence();
-    const unsigned prev = atomicAdd(L.counters + grow, 1u);
-    sh.last = prev == static_cast<unsigned>(ns - 1);
+    out[2] = Gsf;
+    out[3] = 0.0f;
   }
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) sh.last = atomicAdd(L.counters + grow, 1u) == static_cast<unsigned>(ns - 1);
   __syncthreads();
   if (!sh.last) return;
   __threadfence();
 
-  // 3. Last slice block of the row: merge the summaries.
+  // 3. Last slice block of the row: merge the summaries.  Thread b owns the
+  // row bin Gr - b; slice bins below the row's 256 go to `far`.
   const float* sum0 = L.summ + static_cast<int64_t>(sbase) * kSummary;
   float m = -CUDART_INF_F;
-  for (int q = tid; q < ns; q += kSThreads) m = fmaxf(m, __ldcg(sum0 + q * kSummary));
+  for (int q = tid; q < ns; q += kSThreads) m = fmaxf(m, __ldcg(sum0 + static_cast<int64_t>(q) * kSummary));
   m = block_max<kSThreads>(m, sh.red_f);
   const bool empty = !(m > -CUDART_INF_F);
   const float mc = m * c;
@@ -670,80 +624,78 @@ __global__ void __launch_bounds__(kSThreads, 2) topp_slice_kernel(StatsLaunch L)
   int32_t cut = INT32_MAX;
   double K = 0.0;
   if (!empty) {
-    const int G = half_octave(m, c);
-    // Warp w merges slices w, w+8, ...; each lane holds bins lane, lane+32.
-    float b0 = 0.0f, b1 = 0.0f, fsum = 0.0f;
-    for (int q = warp; q < ns; q += kWarps) {
-      const float* sq = sum0 + q * kSummary;
+    const float Grf = floorf(m * c8);
+    unsigned long long acc = 0;
+    float farp = 0.0f;
+#pragma unroll 1
+    for (int q = 0; q < ns; ++q) {
+      const float* sq = sum0 + static_cast<int64_t>(q) * kSummary;
       const float mq = __ldcg(sq);
       if (!(mq > -CUDART_INF_F)) continue;
-      const float f = ex2(fmaf(mq, c, -mc));  // 2^((m_q - m) c)
-      const int D = G - half_octave(mq, c);
-      const int l0 = lane - D, l1 = lane + 32 - D;
-      if (l0 >= 0) b0 += __ldcg(sq + 4 + l0) * f;
-      if (l1 >= 0) b1 += __ldcg(sq + 4 + l1) * f;
-      // Slice bins that fall below the merged window, and the slice's own
-      // mass below its bins.
-      float below = 0.0f;
-      if (lane >= kGB - D) below += __ldcg(sq + 4 + lane);
-      if (lane + 32 >= kGB - D) below += __ldcg(sq + 4 + lane + 32);
-      below = warp_sum(below);
-      fsum += (below + __ldcg(sq + 1)) * f;
+      const float Gq = __ldcg(sq + 2);
+      const int D = static_cast<int>(Grf - Gq);
+      if (tid >= D) acc += static_cast<unsigned long long>(__ldcg(sq + 4 + (tid - D)));
+      if (tid >= kNB - D)  // slice bin Gq - tid lies below the row's bins
+        farp += __ldcg(sq + 4 + tid) * ex2v((Gq - static_cast<float>(tid) + 1.0f) * 0.125f - mc - 21.0f);
+      if (tid == 0) farp += __ldcg(sq + 1) * ex2v(fmaf(mq, c, -mc));
     }
-    sh.mbins[warp][lane] = b0;
-    sh.mbins[warp][lane + 32] = b1;
-    if (lane == 0) sh.mfar[warp] = fsum;
-    __syncthreads();
-    if (warp == 0) {
-      double r0 = 0.0, r1 = 0.0, fr = 0.0;
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
-        r0 += static_cast<double>(sh.mbins[w][2 * lane]);
-        r1 += static_cast<double>(sh.mbins[w][2 * lane + 1]);
-        fr += static_cast<double>(sh.mfar[w]);
-      }
-      const double pair = r0 + r1;
-      double incl = pair;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const double y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      const double tot = __shfl_sync(0xffffffffu, incl, 31) + fr;
-      const double lim = static_cast<double>(L.top_p) * tot;
-      const double before = incl - pair;
-      int hit = -1;
-      double a0 = 0.0;
-      if (before + r0 > lim) {
-        hit = 2 * lane;
-        a0 = before;
-      } else if (before + pair > lim) {
-        hit = 2 * lane + 1;
-        a0 = before + r0;
-      }
-      const unsigned hb = __ballot_sync(0xffffffffu, hit >= 0);
-      const int src = hb ? __ffs(hb) - 1 : 0;
-      const int bs = hb ? __shfl_sync(0xffffffffu, hit, src) : -1;
-      const double a = __shfl_sync(0xffffffffu, a0, src);
-      if (lane == 0) {
-        sh.total = tot;
-        sh.limit = lim;
-        sh.gstar = bs;
-        sh.above0 = a;
-      }
+    // Mass of one unit of bin Gr - b: 2^((Gr - b + 1)/8 - 21 - mc), with the
+    // exponent split into whole and eighth powers of two.
+    if (tid == 0) {
+      const double M = static_cast<double>(mc);
+      sh.unit = exp2(floor(M) - M);
     }
     __syncthreads();
-    const int bstar = sh.gstar;
-    const double limit = sh.limit, above0 = sh.above0, total = sh.total;
+    const int kb = static_cast<int>(Grf) - tid + 1;
+    const int kq = kb >> 3, kr = kb & 7;
+    const double scale = pow2i(kq - static_cast<int>(floor(static_cast<double>(mc))) - 21) * pow2_eighths(kr) * sh.unit;
+    const double mass = static_cast<double>(acc) * scale;
+    double tot;
+    const double excl = block_exclusive_scan_d<kSThreads>(mass, sh.scan, &tot);
+    const double far_all = static_cast<double>(block_sum<kSThreads>(farp, sh.red_f));
+    const double Z = tot + far_all;
+    const double limit = static_cast<double>(L.top_p) * Z;
+    if (tid == 0) sh.gstar = -1;
     __syncthreads();
+    if (mass > 0.0 && excl <= limit && excl + mass > limit) {
+      sh.gstar = tid;
+      sh.above0 = excl;
+      sh.unit = scale * 4.0;  // candidate masses are in units of 2^-19 of the bin's edge
+    }
+    __syncthreads();
+    const int gstar = sh.gstar;
+    const double above0 = sh.above0, unit = sh.unit;
     bool generic = false;
-    if (bstar < 0) {
-      // Nothing in the window reaches top_p * S: every id is kept, or the cut
-      // lies among the masses below the window (exact path).
-      generic = limit < total;
-      if (!generic) K = total;
+    if (gstar < 0) {
+      // Nothing in the 256 bins reaches top_p * S: every id is kept, or the
+      // cut lies among the masses below them (exact path).
+      generic = limit < Z;
+      if (!generic) K = Z;
     } else {
-      generic = !resolve_row<E>(sh, row, S, c, mc, G - bstar, above0, limit, tau, cut, K);
+      // Rescan: the logits of the cut bin with their ids.
+      const float Bf = Grf - static_cast<float>(gstar);
+      const unsigned lane_lt = (1u << lane) - 1u;
+      if (tid == 0) sh.ncand = 0;
+      __syncthreads();
+      for_row<E>(row, S.len, [&](float x, int j) {
+        const bool cand = j >= 0 && floorf(x * c8) == Bf;
+        const unsigned bal = __ballot_sync(0xffffffffu, cand);
+        if (bal) {
+          int base = 0;
+          if (lane == 0) base = atomicAdd(&sh.ncand, __popc(bal));
+          base = __shfl_sync(0xffffffffu, base, 0);
+          const int slot = base + __popc(bal & lane_lt);
+          if (cand && slot < kCandCap) {
+            sh.cand.x[slot] = x;
+            sh.cand.j[slot] = j;
+          }
+        }
+      });
+      __syncthreads();
+      const int n = sh.ncand;
+      generic = n == 0 || n > kCandCap;
+      if (!generic)
+        resolve_candidates<E>(sh, S, c, mc, n, -(Bf + 1.0f) * 0.125f, above0, limit, unit, tau, cut, K);
     }
     if (generic) {
       __syncthreads();
