@@ -39,6 +39,8 @@ constexpr int kNB = 256;                        // eighth-octave bins under a sl
 constexpr int kSummary = 4 + kNB;               // floats per slice summary
 constexpr int kCandCap = 4096;                  // candidates of the cut bin in shared memory
 constexpr int kFinal = 64;
+constexpr int kMaxStaged = kCandCap / 2;         // slice headers staged in shared memory
+constexpr int kRegion = kCandCap / (kSThreads / 32);  // candidates per warp in the rescan
 constexpr int kWarps = kSThreads / 32;
 constexpr float kFixBin = 2097152.0f;           // 2^21: slice bin masses, units of the bin's upper edge
 constexpr float kFixCand = 524288.0f;           // 2^19: candidate level masses
@@ -73,6 +75,7 @@ struct ToppShared {
   int pick_sec;
   unsigned pick_key;
   double above0, limit, total, kept_mass, unit;
+  float xlo, xhi;
 };
 
 // exp2 that the compiler may not merge with an identical earlier one.
@@ -141,6 +144,59 @@ __device__ __forceinline__ void for_row(const E* row, int len, F&& f) {
     const int j = t < rs.head ? t : (t < rs.head + ntail ? rs.tail0 + (t - rs.head) : -1);
     f(j >= 0 ? Elem<E>::load(row + j) : -CUDART_INF_F, j);
   }
+}
+
+// Visit every logit of a row with the loads of the next batch of 16-byte
+// vectors issued before the current batch is used; f(value, index), index -1
+// for padding.  Block-uniform trip counts (f may use full-warp votes).
+template <typename E, typename F>
+__device__ __forceinline__ void scan_row(const E* row, int len, F&& f) {
+  constexpr int EPV = Elem<E>::kPerVec;
+  constexpr int U = 4;
+  constexpr int kStep = kSThreads * U;
+  const RowSplit rs = split_row(row, len);
+  const uint4* vp = reinterpret_cast<const uint4*>(row + rs.head);
+  const int v0 = static_cast<int>(threadIdx.x);
+  auto load = [&](uint4* w, int base) {
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int v = base + v0 + u * kSThreads;
+      w[u] = v < rs.nvec ? __ldcg(vp + v) : Elem<E>::neg_inf_vec();
+    }
+  };
+  auto use = [&](const uint4* w, int base) {
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int v = base + v0 + u * kSThreads;
+#pragma unroll
+      for (int i = 0; i < EPV; ++i) f(Elem<E>::at(w[u], i), v < rs.nvec ? rs.head + v * EPV + i : -1);
+    }
+  };
+  uint4 a[U], b[U];
+  if (rs.nvec > 0) load(a, 0);
+  for (int base = 0; base < rs.nvec; base += 2 * kStep) {
+    if (base + kStep < rs.nvec) load(b, base + kStep);
+    use(a, base);
+    if (base + kStep >= rs.nvec) break;
+    if (base + 2 * kStep < rs.nvec) load(a, base + 2 * kStep);
+    use(b, base + kStep);
+  }
+  const int ntail = len - rs.tail0;
+  for (int t0 = 0; t0 < rs.head + ntail; t0 += kSThreads) {
+    const int t = t0 + static_cast<int>(threadIdx.x);
+    const int j = t < rs.head ? t : (t < rs.head + ntail ? rs.tail0 + (t - rs.head) : -1);
+    f(j >= 0 ? Elem<E>::load(row + j) : -CUDART_INF_F, j);
+  }
+}
+
+// The smallest float x with floor(x * c8) >= b (c8 > 0): x * c8 rounds
+// monotonically, so the logits with floor(x * c8) == b are exactly
+// [first_at_or_above(b), first_at_or_above(b + 1)).
+__device__ __forceinline__ float first_at_or_above(float b, float c8) {
+  float x = b / c8;
+  for (int i = 0; i < 64 && x * c8 >= b; ++i) x = nextafterf(x, -CUDART_INF_F);
+  for (int i = 0; i < 64 && x * c8 < b; ++i) x = nextafterf(x, CUDART_INF_F);
+  return x;
 }
 
 // Warp 0: first bin from `top` down to 0 where above + mass > limit; if none,
@@ -356,79 +412,96 @@ __device__ void resolve_candidates(ToppShared& sh, const RowSet& S, float c, flo
                                    double above0, double limit, double unit, uint32_t& tau, int32_t& cut,
                                    double& K) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const unsigned lane_lt = (1u << lane) - 1u;
-  uint32_t kmin = 0xffffffffu, kmax = 0u;
-  for (int i = tid; i < n; i += kSThreads) {
-    const uint32_t k = order_key(sh.cand.x[i]);
-    kmin = min(kmin, k);
-    kmax = max(kmax, k);
-  }
-  kmax = static_cast<uint32_t>(block_max_u64<kSThreads>(kmax, sh.red_u));
-  kmin = 0xffffffffu - static_cast<uint32_t>(block_max_u64<kSThreads>(0xffffffffu - kmin, sh.red_u));
-  const double lim_rel = limit - above0;
-  const unsigned long long lim_f = lim_rel > 0.0 ? static_cast<unsigned long long>(lim_rel / unit) : 0ull;
   unsigned long long above_f = 0;
-  uint32_t kbase = kmin;
-  const uint32_t span = kmax - kmin;
-  int shift = span ? max(0, 32 - __clz(static_cast<int>(span)) - 8) : 0;
+  uint32_t kbase = 0;
   int cnt = n;
+  if (n > kFinal) {
+    uint32_t kmin = 0xffffffffu, kmax = 0u;
+    for (int i = tid; i < n; i += kSThreads) {
+      const uint32_t k = order_key(sh.cand.x[i]);
+      kmin = min(kmin, k);
+      kmax = max(kmax, k);
+    }
+    kmax = static_cast<uint32_t>(block_max_u64<kSThreads>(kmax, sh.red_u));
+    kmin = 0xffffffffu - static_cast<uint32_t>(block_max_u64<kSThreads>(0xffffffffu - kmin, sh.red_u));
+    const double lim_rel = limit - above0;
+    const unsigned long long lim_f = lim_rel > 0.0 ? static_cast<unsigned long long>(lim_rel / unit) : 0ull;
+    kbase = kmin;
+    const uint32_t span = kmax - kmin;
+    int shift = span ? max(0, 32 - __clz(static_cast<int>(span)) - 8) : 0;
 #pragma unroll 1
-  for (;;) {
-    for (int t = tid; t < 256; t += kSThreads) {
-      sh.hcnt[t] = 0u;
-      sh.hmass[t] = 0u;
-    }
-    __syncthreads();
-    for (int i = tid; i < cnt; i += kSThreads) {
-      const float x = sh.cand.x[i];
-      const uint32_t d = (order_key(x) - kbase) >> shift;
-      atomicAdd(&sh.hcnt[d], 1u);
-      atomicAdd(&sh.hmass[d], __float2uint_rn(ex2v(fmaf(x, c, nb)) * kFixCand));
-    }
-    __syncthreads();
-    for (int t = tid; t < 256; t += kSThreads) {
-      sh.tcnt[t] = sh.hcnt[t];
-      sh.tmass[t] = sh.hmass[t];
-    }
-    __syncthreads();
-    crossing_desc(sh, 255, above_f, lim_f);
-    __syncthreads();
-    const uint32_t dsel = static_cast<uint32_t>(sh.sel);
-    above_f = sh.sel_above;
-    // Keep the candidates of digit dsel, in order, in place: chunks of one
-    // entry per thread, each read completely before any of it is written.
-    int kept_n = 0;
-    for (int b0 = 0; b0 < cnt; b0 += kSThreads) {
-      const int i = b0 + tid;
-      bool keep = false;
-      float xv = 0.0f;
-      int jv = 0;
-      if (i < cnt) {
-        xv = sh.cand.x[i];
-        jv = sh.cand.j[i];
-        keep = ((order_key(xv) - kbase) >> shift) == dsel;
+    for (;;) {
+      for (int t = tid; t < 256; t += kSThreads) {
+        sh.hcnt[t] = 0u;
+        sh.hmass[t] = 0u;
       }
-      const unsigned bal = __ballot_sync(0xffffffffu, keep);
-      if (lane == 0) sh.wcnt[warp] = __popc(bal);
       __syncthreads();
-      int off = kept_n, chunk = 0;
+      for (int i = tid; i < cnt; i += kSThreads) {
+        const float x = sh.cand.x[i];
+        const uint32_t d = (order_key(x) - kbase) >> shift;
+        atomicAdd(&sh.hcnt[d], 1u);
+        atomicAdd(&sh.hmass[d], __float2uint_rn(ex2v(fmaf(x, c, nb)) * kFixCand));
+      }
+      __syncthreads();
+      for (int t = tid; t < 256; t += kSThreads) {
+        sh.tcnt[t] = sh.hcnt[t];
+        sh.tmass[t] = sh.hmass[t];
+      }
+      __syncthreads();
+      crossing_desc(sh, 255, above_f, lim_f);
+      __syncthreads();
+      const uint32_t dsel = static_cast<uint32_t>(sh.sel);
+      above_f = sh.sel_above;
+      // Keep the candidates of digit dsel, in order, in place: chunks of four
+      // entries per thread, each read completely before any of it is written.
+      int kept_n = 0;
+      for (int b0 = 0; b0 < cnt; b0 += 4 * kSThreads) {
+        float xv[4];
+        int jv[4];
+        unsigned km = 0;
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
-        const int nw = sh.wcnt[w];
-        if (w < warp) off += nw;
-        chunk += nw;
+        for (int r = 0; r < 4; ++r) {
+          const int i = b0 + 4 * tid + r;
+          xv[r] = 0.0f;
+          jv[r] = 0;
+          if (i < cnt) {
+            xv[r] = sh.cand.x[i];
+            jv[r] = sh.cand.j[i];
+            if (((order_key(xv[r]) - kbase) >> shift) == dsel) km |= 1u << r;
+          }
+        }
+        const int k = __popc(km);
+        int incl = k;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        if (lane == 31) sh.wcnt[warp] = incl;
+        __syncthreads();
+        int off = kept_n + incl - k, chunk = 0;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+          const int nw = sh.wcnt[w];
+          if (w < warp) off += nw;
+          chunk += nw;
+        }
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          if (km & (1u << r)) {
+            sh.cand.x[off] = xv[r];
+            sh.cand.j[off] = jv[r];
+            ++off;
+          }
+        }
+        kept_n += chunk;
+        __syncthreads();
       }
-      if (keep) {
-        sh.cand.x[off + __popc(bal & lane_lt)] = xv;
-        sh.cand.j[off + __popc(bal & lane_lt)] = jv;
-      }
-      kept_n += chunk;
-      __syncthreads();
+      cnt = kept_n;
+      kbase += dsel << shift;
+      if (cnt <= kFinal || shift == 0) break;
+      shift = max(0, shift - 8);
     }
-    cnt = kept_n;
-    kbase += dsel << shift;
-    if (cnt <= kFinal || shift == 0) break;
-    shift = max(0, shift - 8);
   }
   const double above = above0 + static_cast<double>(above_f) * unit;
   if (cnt <= kFinal) {
@@ -452,23 +525,30 @@ __device__ void resolve_candidates(ToppShared& sh, const RowSet& S, float c, flo
       if (lane < cnt) sh.gidx[ra] = lane;
       if (lane + 32 < cnt) sh.gidx[rb] = lane + 32;
       __syncwarp();
-      if (lane == 0) {
-        double cum = above;
-        int pick = cnt - 1;
-        for (int r = 0; r < cnt; ++r) {
-          const double e = static_cast<double>(weight(sh.cand.x[sh.gidx[r]], c, mc));
-          if (cum + e > limit) {
-            pick = r;
-            break;
-          }
-          cum += e;
+      // Masses in sorted order (lane r: ranks r and r + 32), prefix sums in
+      // double, the first rank whose inclusive mass exceeds the limit.
+      double i0 = lane < cnt ? static_cast<double>(weight(sh.cand.x[sh.gidx[lane]], c, mc)) : 0.0;
+      double i1 = lane + 32 < cnt ? static_cast<double>(weight(sh.cand.x[sh.gidx[lane + 32]], c, mc)) : 0.0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const double y0 = __shfl_up_sync(0xffffffffu, i0, o);
+        const double y1 = __shfl_up_sync(0xffffffffu, i1, o);
+        if (lane >= o) {
+          i0 += y0;
+          i1 += y1;
         }
-        double kept_mass = above;
-        for (int r = 0; r <= pick; ++r) kept_mass += static_cast<double>(weight(sh.cand.x[sh.gidx[r]], c, mc));
+      }
+      i1 += __shfl_sync(0xffffffffu, i0, 31);
+      const unsigned h0 = __ballot_sync(0xffffffffu, lane < cnt && above + i0 > limit);
+      const unsigned h1 = __ballot_sync(0xffffffffu, lane + 32 < cnt && above + i1 > limit);
+      const int pick = h0 ? __ffs(h0) - 1 : (h1 ? 31 + __ffs(h1) : cnt - 1);
+      const double ip0 = __shfl_sync(0xffffffffu, i0, pick & 31);
+      const double ip1 = __shfl_sync(0xffffffffu, i1, pick & 31);
+      if (lane == 0) {
         const int ip = sh.gidx[pick];
         sh.pick_key = order_key(sh.cand.x[ip]);
         sh.pick_sec = tie_key(S, sh.cand.j[ip]);
-        sh.kept_mass = kept_mass;
+        sh.kept_mass = above + (pick < 32 ? ip0 : ip1);
       }
     }
     __syncthreads();
@@ -592,7 +672,7 @@ __global__ void __launch_bounds__(kSThreads, 3) topp_slice_kernel(StatsLaunch L)
   __syncthreads();
   // Publish: slot t holds bin Gs - t.
   float* out = L.summ + static_cast<int64_t>(sbase + s) * kSummary;
-  {
+  if (tid < kNB) {
     unsigned long long a = 0;
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) a += sh.wh[w][tid];
@@ -627,28 +707,62 @@ __global__ void __launch_bounds__(kSThreads, 3) topp_slice_kernel(StatsLaunch L)
     const float Grf = floorf(m * c8);
     unsigned long long acc = 0;
     float farp = 0.0f;
+    if (ns <= kMaxStaged) {
+      // Slice headers staged in shared memory, then every bin load of every
+      // slice issued independently.
+      float* hg = sh.cand.x;                          // slice top bin
+      int* hd = sh.cand.j;                            // row top bin - slice top bin (huge: empty)
+      for (int q = tid; q < ns; q += kSThreads) {
+        const float* sq = sum0 + static_cast<int64_t>(q) * kSummary;
+        const float mq = __ldcg(sq);
+        const float Gq = __ldcg(sq + 2);
+        const bool lq = mq > -CUDART_INF_F;
+        hg[q] = Gq;
+        hd[q] = lq ? static_cast<int>(Grf - Gq) : (1 << 24);
+        if (lq) farp += __ldcg(sq + 1) * ex2v(fmaf(mq, c, -mc));
+      }
+      __syncthreads();
+      // Eight slices at a time, every load issued before any is used.
 #pragma unroll 1
-    for (int q = 0; q < ns; ++q) {
-      const float* sq = sum0 + static_cast<int64_t>(q) * kSummary;
-      const float mq = __ldcg(sq);
-      if (!(mq > -CUDART_INF_F)) continue;
-      const float Gq = __ldcg(sq + 2);
-      const int D = static_cast<int>(Grf - Gq);
-      if (tid >= D) acc += static_cast<unsigned long long>(__ldcg(sq + 4 + (tid - D)));
-      if (tid >= kNB - D)  // slice bin Gq - tid lies below the row's bins
-        farp += __ldcg(sq + 4 + tid) * ex2v((Gq - static_cast<float>(tid) + 1.0f) * 0.125f - mc - 21.0f);
-      if (tid == 0) farp += __ldcg(sq + 1) * ex2v(fmaf(mq, c, -mc));
+      for (int q0 = 0; q0 < ns; q0 += 8) {
+        float v[8], w[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int q = q0 + u;
+          const int D = q < ns ? hd[q] : (1 << 24);
+          const float* sq = sum0 + static_cast<int64_t>(q < ns ? q : 0) * kSummary + 4;
+          v[u] = (tid >= D && tid < kNB) ? __ldcg(sq + (tid - D)) : 0.0f;
+          // Slice bin Gq - tid lies below the row's bins.
+          w[u] = (D < (1 << 24) && tid >= kNB - D && tid < kNB) ? __ldcg(sq + tid) : 0.0f;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          acc += static_cast<unsigned long long>(v[u]);
+          if (w[u] > 0.0f)
+            farp += w[u] * ex2v((hg[q0 + u] - static_cast<float>(tid) + 1.0f) * 0.125f - mc - 21.0f);
+        }
+      }
+    } else {
+#pragma unroll 1
+      for (int q = 0; q < ns; ++q) {
+        const float* sq = sum0 + static_cast<int64_t>(q) * kSummary;
+        const float mq = __ldcg(sq);
+        if (!(mq > -CUDART_INF_F)) continue;
+        const float Gq = __ldcg(sq + 2);
+        const int D = static_cast<int>(Grf - Gq);
+        if (tid >= D && tid < kNB) acc += static_cast<unsigned long long>(__ldcg(sq + 4 + (tid - D)));
+        if (tid >= kNB - D && tid < kNB)
+          farp += __ldcg(sq + 4 + tid) * ex2v((Gq - static_cast<float>(tid) + 1.0f) * 0.125f - mc - 21.0f);
+        if (tid == 0) farp += __ldcg(sq + 1) * ex2v(fmaf(mq, c, -mc));
+      }
     }
     // Mass of one unit of bin Gr - b: 2^((Gr - b + 1)/8 - 21 - mc), with the
     // exponent split into whole and eighth powers of two.
-    if (tid == 0) {
-      const double M = static_cast<double>(mc);
-      sh.unit = exp2(floor(M) - M);
-    }
+    if (tid == 0) sh.unit = static_cast<double>(ex2v(floorf(mc) - mc));
     __syncthreads();
     const int kb = static_cast<int>(Grf) - tid + 1;
     const int kq = kb >> 3, kr = kb & 7;
-    const double scale = pow2i(kq - static_cast<int>(floor(static_cast<double>(mc))) - 21) * pow2_eighths(kr) * sh.unit;
+    const double scale = pow2i(kq - static_cast<int>(floorf(mc)) - 21) * pow2_eighths(kr) * sh.unit;
     const double mass = static_cast<double>(acc) * scale;
     double tot;
     const double excl = block_exclusive_scan_d<kSThreads>(mass, sh.scan, &tot);
@@ -672,25 +786,83 @@ __global__ void __launch_bounds__(kSThreads, 3) topp_slice_kernel(StatsLaunch L)
       generic = limit < Z;
       if (!generic) K = Z;
     } else {
-      // Rescan: the logits of the cut bin with their ids.
+      // Rescan: the logits of the cut bin with their ids, each warp into its
+      // own region of the list; if a region overflows, again with one
+      // shared counter.
       const float Bf = Grf - static_cast<float>(gstar);
       const unsigned lane_lt = (1u << lane) - 1u;
-      if (tid == 0) sh.ncand = 0;
+      // floor(l * c8) == Bf exactly for the logits in [xlo, xhi).
+      if (tid == 0) {
+        sh.xlo = first_at_or_above(Bf, c8);
+        sh.xhi = first_at_or_above(Bf + 1.0f, c8);
+      }
       __syncthreads();
-      for_row<E>(row, S.len, [&](float x, int j) {
-        const bool cand = j >= 0 && floorf(x * c8) == Bf;
+      const float xlo = sh.xlo, xhi = sh.xhi;
+      int wn = 0;
+      scan_row<E>(row, S.len, [&](float x, int j) {
+        const bool cand = x >= xlo && x < xhi;
         const unsigned bal = __ballot_sync(0xffffffffu, cand);
         if (bal) {
-          int base = 0;
-          if (lane == 0) base = atomicAdd(&sh.ncand, __popc(bal));
-          base = __shfl_sync(0xffffffffu, base, 0);
-          const int slot = base + __popc(bal & lane_lt);
-          if (cand && slot < kCandCap) {
-            sh.cand.x[slot] = x;
-            sh.cand.j[slot] = j;
+          const int slot = wn + __popc(bal & lane_lt);
+          if (cand && slot < kRegion) {
+            sh.cand.x[warp * kRegion + slot] = x;
+            sh.cand.j[warp * kRegion + slot] = j;
           }
+          wn += __popc(bal);
         }
       });
+      if (lane == 0) sh.wcnt[warp] = wn;
+      __syncthreads();
+      int total_c = 0, my_off = 0, over = 0;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        const int nw = sh.wcnt[w];
+        over |= nw > kRegion;
+        if (w < warp) my_off += nw;
+        total_c += nw;
+      }
+      if (!over) {
+        // Pack the regions to the front in warp order: every entry is read
+        // into registers before any is written.
+        constexpr int kPer = kRegion / 32;
+        float rx[kPer];
+        int rj[kPer];
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+          const int e2 = lane + 32 * k;
+          rx[k] = e2 < wn ? sh.cand.x[warp * kRegion + e2] : 0.0f;
+          rj[k] = e2 < wn ? sh.cand.j[warp * kRegion + e2] : 0;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+          const int e2 = lane + 32 * k;
+          if (e2 < wn) {
+            sh.cand.x[my_off + e2] = rx[k];
+            sh.cand.j[my_off + e2] = rj[k];
+          }
+        }
+        if (tid == 0) sh.ncand = total_c;
+      } else if (total_c <= kCandCap) {
+        if (tid == 0) sh.ncand = 0;
+        __syncthreads();
+        scan_row<E>(row, S.len, [&](float x, int j) {
+          const bool cand = x >= xlo && x < xhi;
+          const unsigned bal = __ballot_sync(0xffffffffu, cand);
+          if (bal) {
+            int base = 0;
+            if (lane == 0) base = atomicAdd(&sh.ncand, __popc(bal));
+            base = __shfl_sync(0xffffffffu, base, 0);
+            const int slot = base + __popc(bal & lane_lt);
+            if (cand && slot < kCandCap) {
+              sh.cand.x[slot] = x;
+              sh.cand.j[slot] = j;
+            }
+          }
+        });
+      } else if (tid == 0) {
+        sh.ncand = total_c;
+      }
       __syncthreads();
       const int n = sh.ncand;
       generic = n == 0 || n > kCandCap;
