@@ -411,7 +411,7 @@ def run_ours(args, dist: Dist):
     dom_name = {True: "greedy_kernel(tree)", False: None}[R.tree]
     if not R.tree:
         dom_name = "greedy_kernel(chain)" if cfg.temperature == 0 else (
-            "stats_resident_kernel" if cfg.top_p < 1 else "stats_stream_kernel")
+            "topp_slice_kernel" if cfg.top_p < 1 else "stats_stream_kernel")
     achieved = step_bytes(cfg) / (avg_phase[dom] / 1e3) / 1e9
     traffic = ncu_traffic(args.workload, dom_name)
     res = {
