@@ -133,7 +133,7 @@ def ncu_traffic(workload: str, kernel: str):
         lines = open(path).read().splitlines()
     except OSError:
         return None
-    src = source_hash()
+    src = source_hash(kernel)
     for ln in lines:
         cells = [c.strip() for c in ln.strip().strip("|").split("|")]
         if len(cells) >= 4 and cells[0] == workload and cells[1] == kernel:
@@ -145,11 +145,23 @@ def ncu_traffic(workload: str, kernel: str):
     return None
 
 
-def source_hash() -> str:
+KERNEL_SOURCES = {
+    "topp_slice_kernel": "sv_topp.cu",
+    "stats_stream_kernel": "sv_chain.cu",
+    "decide_kernel": "sv_decide.cu",
+    "greedy_kernel(chain)": "sv_greedy.cu",
+    "greedy_kernel(tree)": "sv_greedy.cu",
+}
+
+
+def source_hash(kernel: str | None = None) -> str:
+    """Hash of the sources a kernel is built from: its .cu file and the
+    shared headers (every source when the kernel is not listed)."""
     d = os.path.join(ROOT, "draft_token_verification_sv_gb300", "csrc")
+    own = KERNEL_SOURCES.get(kernel) if kernel else None
     h = hashlib.sha256()
     for name in sorted(os.listdir(d)):
-        if name.endswith((".cu", ".cuh", ".h")):
+        if name.endswith((".cuh", ".h")) or (name.endswith(".cu") and (own is None or name == own)):
             h.update(name.encode())
             h.update(open(os.path.join(d, name), "rb").read())
     return h.hexdigest()[:12]

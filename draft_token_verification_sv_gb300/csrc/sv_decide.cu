@@ -25,7 +25,7 @@ constexpr int kDThreads = 256;
 constexpr int kDEPT = 8;                    // consecutive ids per thread per chunk
 constexpr int kDChunk = kDThreads * kDEPT;  // 2048 ids per chunk
 constexpr int kDWarps = kDThreads / 32;
-constexpr int kDMaxNC = 8;                  // chunks per block: 8 for two bf16 rows, else 4
+constexpr int kDMaxNC = 8;                  // chunks per block (at most)
 
 struct DrawSide {
   float mc, invK;
@@ -478,14 +478,44 @@ static sv_status launch_decide_typed(DecideParams P, void* scratch, cudaStream_t
   return SV_OK;
 }
 
+// Chunks per block: the most (8 for two bf16 rows, else 4) that still gives
+// the launch about four blocks per SM; fewer chunks per block otherwise, so
+// small batches still spread over the GPU.
+static int chunks_per_block(int B, int V, int nc_max) {
+  static int sms[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+  if (sms[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    sms[dev] = n;
+  }
+  const long long want = 4LL * sms[dev];
+  const int nchunks = (V + kDChunk - 1) / kDChunk;
+  int nc = nc_max;
+  while (nc > 2 && static_cast<long long>(B) * ((nchunks + nc - 1) / nc) < want) nc /= 2;
+  return nc;
+}
+
 sv_status launch_decide(const DecideParams& P, sv_dtype td, sv_dtype dd, void* scratch, cudaStream_t stream) {
   if (P.B == 0) return SV_OK;
   const bool tb = td == SV_BF16, db = dd == SV_BF16;
-  if (tb && db && !P.t2d) return launch_decide_typed<uint16_t, uint16_t, 8>(P, scratch, stream);
-  if (tb && db) return launch_decide_typed<uint16_t, uint16_t, 4>(P, scratch, stream);
-  if (tb) return launch_decide_typed<uint16_t, float, 4>(P, scratch, stream);
-  if (db) return launch_decide_typed<float, uint16_t, 4>(P, scratch, stream);
-  return launch_decide_typed<float, float, 4>(P, scratch, stream);
+  const int nc = chunks_per_block(P.B, P.V, tb && db && !P.t2d ? 8 : 4);
+  if (tb && db) {
+    if (nc == 8) return launch_decide_typed<uint16_t, uint16_t, 8>(P, scratch, stream);
+    if (nc == 4) return launch_decide_typed<uint16_t, uint16_t, 4>(P, scratch, stream);
+    return launch_decide_typed<uint16_t, uint16_t, 2>(P, scratch, stream);
+  }
+  if (tb) {
+    if (nc == 4) return launch_decide_typed<uint16_t, float, 4>(P, scratch, stream);
+    return launch_decide_typed<uint16_t, float, 2>(P, scratch, stream);
+  }
+  if (db) {
+    if (nc == 4) return launch_decide_typed<float, uint16_t, 4>(P, scratch, stream);
+    return launch_decide_typed<float, uint16_t, 2>(P, scratch, stream);
+  }
+  if (nc == 4) return launch_decide_typed<float, float, 4>(P, scratch, stream);
+  return launch_decide_typed<float, float, 2>(P, scratch, stream);
 }
 
 }  // namespace sv
