@@ -12,13 +12,13 @@
 // Two passes over device memory:
 //   1. statistics: one pass over every logit row computes the row maximum,
 //      the softmax normaliser and, when top_p < 1, the exact top-p threshold
-//      (radix select over order keys with integer masses, rows held in the
-//      shared memory of a thread-block cluster); it also evaluates the row's
-//      weight at its draft id.
-//   2. decision: one block per batch row turns those into p(x), q(x), finds
-//      the first rejection and draws the resample/bonus token by an inverse
-//      CDF over one (pair of) rows: chunk sums, then a block scan of the one
-//      chunk that holds the draw.
+//      (sv_topp.cu); it also evaluates the row's weight at its draft id.  In
+//      the top-p pass, the block that writes the last statistic of a batch
+//      row makes that row's accept/reject decisions (one warp) and records
+//      the draw rows; without top-p the draw makes them.
+//   2. draw (sv_decide.cu): blocks over segments of the vocabulary sum the
+//      draw weights of the recorded rows per chunk; the last block of a batch
+//      row draws by an inverse CDF within the one chunk that holds u * total.
 #include "sv_rows.cuh"
 
 #include <algorithm>
@@ -109,6 +109,17 @@ __global__ void __launch_bounds__(THREADS) stats_stream_kernel(StatsLaunch L) {
       st.e_query = weight(Elem<E>::load(row + q.elem), c, st.mc);
     S.out[r] = st;
   }
+  // Warp 0 alone (thread 0 wrote the statistics): count the row for its
+  // batch row and, after the batch row's last one, make its decisions.
+  if (L.dec.rec && threadIdx.x < 32) {
+    bool last = false;
+    if (threadIdx.x == 0) last = count_row(L.dec, S, r);
+    if (__shfl_sync(0xffffffffu, last, 0)) {
+      __threadfence();
+      const DecideRecord rc = decide_batch(L.dec, r / S.per_group);
+      if ((threadIdx.x & 31) == 0) L.dec.rec[r / S.per_group] = rc;
+    }
+  }
 }
 
 // ------------------------------------------------------------------ host ----
@@ -190,7 +201,26 @@ sv_status sampling_chain(const ChainArgs& a, cudaStream_t stream) {
     L.nsets = 2;
     max_len = std::max(max_len, d.draft_vocab);
   }
+  DecideRecord* rec = reinterpret_cast<DecideRecord*>(static_cast<char*>(a.workspace) + WL.records);
+  unsigned* bcount = reinterpret_cast<unsigned*>(static_cast<char*>(a.workspace) + WL.counters);
+  L.dec.t_stats = stats;
+  L.dec.d_stats = stats + static_cast<int64_t>(B) * (G + 1);
+  L.dec.ids = a.ids;
+  L.dec.u_accept = a.u_accept;
+  L.dec.p_draft = a.p_draft;
+  L.dec.q_draft = a.q_draft;
+  L.dec.rec = rec;
+  L.dec.counters = bcount;
+  L.dec.G = G;
+  L.dec.V = d.vocab;
+  L.dec.rows_per_batch = 2 * G + 1;
+  // The top-p pass has a last block per row: it makes the decisions of a
+  // batch row after the row's last statistic.  Otherwise the draw does.
+  DecideIn in_draw = L.dec;
+  if (!resident) L.dec.rec = nullptr;
   start_phases(stream);
+  if (resident && cudaMemsetAsync(bcount, 0, static_cast<size_t>(B) * sizeof(unsigned), stream) != cudaSuccess)
+    return SV_ERR_CUDA;
   void* scratch = static_cast<char*>(a.workspace) + WL.topp;
   sv_status s = launch_stats_sets(L, d.target_dtype, d.draft_dtype, resident, scratch, stream);
   if (s != SV_OK) return s;
@@ -204,16 +234,13 @@ sv_status sampling_chain(const ChainArgs& a, cudaStream_t stream) {
   P.V = d.vocab;
   P.Vd = d.draft_vocab;
   P.c = L.c;
-  P.t_stats = stats;
-  P.d_stats = stats + static_cast<int64_t>(B) * (G + 1);
+  P.rec = resident ? rec : nullptr;
+  P.dec = in_draw;
   P.ids = a.ids;
-  P.u_accept = a.u_accept;
   P.u_resample = a.u_resample;
   P.t2d = a.d2t ? a.t2d : nullptr;
   P.out_tokens = a.out_tokens;
   P.num_accepted = a.num_accepted;
-  P.p_draft = a.p_draft;
-  P.q_draft = a.q_draft;
   P.row_status = a.row_status;
   return launch_decide(P, d.target_dtype, d.draft_dtype, static_cast<char*>(a.workspace) + WL.decide, stream);
 }
@@ -237,9 +264,23 @@ sv_status sample_rows(const sv_sample_desc& d, const void* logits, const float* 
   T.ids = nullptr;
   T.vocab = d.vocab;
   T.out = stats;
+  DecideRecord* rec = reinterpret_cast<DecideRecord*>(static_cast<char*>(workspace) + sample_records_offset(d.rows));
+  unsigned* bcount = reinterpret_cast<unsigned*>(static_cast<char*>(workspace) + sample_counters_offset(d.rows));
+  L.dec.t_stats = stats;
+  L.dec.d_stats = stats;
+  L.dec.rec = rec;
+  L.dec.counters = bcount;
+  L.dec.G = 0;
+  L.dec.V = d.vocab;
+  L.dec.rows_per_batch = 1;
+  const bool resident = d.top_p < 1.0f;
+  DecideIn in_draw = L.dec;
+  if (!resident) L.dec.rec = nullptr;
   start_phases(stream);
-  void* scratch = static_cast<char*>(workspace) + sample_stats_bytes(d.rows);
-  sv_status s = launch_stats_sets(L, d.dtype, d.dtype, d.top_p < 1.0f, scratch, stream);
+  if (resident && cudaMemsetAsync(bcount, 0, static_cast<size_t>(d.rows) * sizeof(unsigned), stream) != cudaSuccess)
+    return SV_ERR_CUDA;
+  void* scratch = static_cast<char*>(workspace) + sample_topp_offset(d.rows);
+  sv_status s = launch_stats_sets(L, d.dtype, d.dtype, resident, scratch, stream);
   if (s != SV_OK) return s;
   DecideParams P{};
   P.target = logits;
@@ -248,13 +289,13 @@ sv_status sample_rows(const sv_sample_desc& d, const void* logits, const float* 
   P.G = 0;
   P.V = d.vocab;
   P.c = L.c;
-  P.t_stats = stats;
-  P.d_stats = stats;
+  P.rec = resident ? rec : nullptr;
+  P.dec = in_draw;
   P.u_resample = u;
   P.out_tokens = out_tokens;
   P.out_prob = out_prob;
   return launch_decide(P, d.dtype, d.dtype,
-                       static_cast<char*>(workspace) + sample_stats_bytes(d.rows) + sample_topp_bytes(d), stream);
+                       static_cast<char*>(workspace) + sample_topp_offset(d.rows) + sample_topp_bytes(d), stream);
 }
 
 }  // namespace sv
@@ -306,7 +347,7 @@ sv_status probs_rows(const sv_sample_desc& d, const void* logits, float* out, in
   T.vocab = d.vocab;
   T.out = stats;
   start_phases(stream);
-  void* scratch = static_cast<char*>(workspace) + sample_stats_bytes(d.rows);
+  void* scratch = static_cast<char*>(workspace) + sample_topp_offset(d.rows);
   sv_status s = launch_stats_sets(L, d.dtype, d.dtype, d.top_p < 1.0f, scratch, stream);
   if (s != SV_OK) return s;
   const int tiles = (d.vocab + 2047) / 2048;

@@ -7,16 +7,19 @@
 // acceptances sample the extra token from p) and §4.2 (the accept loop of
 // generate()).  The uniforms are supplied by the caller.
 //
-// The vocabulary of a batch row is cut into segments of NC chunks of 2048
-// ids, one thread block per (row, segment), with no cooperation between the
-// blocks of a row while they stream.  Every block first evaluates the row's
-// decisions (a few scalars per draft, from the statistics pass) to learn the
-// draw position k, then loads its segment of target row k (and of draft row
-// k when drawing from the residual) with every 16-byte load of the segment
-// issued before the first is used, and writes one draw-weight sum per chunk.
-// The last block of the row to finish (a counter per row) scans the chunk
-// sums, finds the chunk that holds u * total and rescans that one chunk
-// (from L2) with a block-wide prefix scan to pick the token.
+// The accept/reject decisions of a batch row (decide_batch in sv_rows.cuh:
+// the first rejection k, the status bits and the draw rows) are made by the
+// statistics pass when it has a last block per row anyway (top-p), else by
+// warp 0 of every block here.  The vocabulary
+// of a batch row is cut into segments of NC chunks of 2048 ids, one thread
+// block per (row, segment), with no cooperation between the blocks of a row
+// while they stream.  Every block reads the record, then loads its segment of
+// target row k (and of draft row k when drawing from the residual) with every
+// 16-byte load of the segment issued before the first is used, and writes one
+// draw-weight sum per chunk.  The last block of the row to finish (a counter
+// per row) scans the chunk sums, finds the chunk that holds u * total and
+// rescans that one chunk (from L2) with a block-wide prefix scan to pick the
+// token.
 #include "sv_rows.cuh"
 
 namespace sv {
@@ -27,13 +30,8 @@ constexpr int kDChunk = kDThreads * kDEPT;  // 2048 ids per chunk
 constexpr int kDWarps = kDThreads / 32;
 constexpr int kDMaxNC = 8;                  // chunks per block (at most)
 
-struct DrawSide {
-  float mc, invK;
-  uint32_t tau;
-  int32_t cut;
-};
-
 struct DecideShared {
+  DecideRecord rec;
   float wsum[kDMaxNC][kDWarps];
   DrawSide pt, pd;
   double scan[32];
@@ -69,10 +67,6 @@ __device__ __forceinline__ float raw_at(const Raw8<E>& r, int e) {
   } else {
     return Elem<float>::at(r.v[e >> 2], e & 3);
   }
-}
-
-__device__ __forceinline__ DrawSide draw_side(const RowStats& s) {
-  return DrawSide{s.mc, s.K > 0.0 ? static_cast<float>(1.0 / s.K) : 0.0f, s.tau, s.cut};
 }
 
 // Normalised filtered probability of id j with logit x (0 if filtered out).
@@ -220,49 +214,18 @@ __global__ void __launch_bounds__(kDThreads, 2) decide_kernel(DecideParams P, in
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = P.G, V = P.V;
   const int nchunks = (V + kDChunk - 1) / kDChunk;
-  const RowStats* ts = P.t_stats + static_cast<int64_t>(b) * (G + 1);
-  const RowStats* ds = P.d_stats + static_cast<int64_t>(b) * G;
 
-  // Decisions (identical in every block of the row), by warp 0: accept
-  // draft i iff u_i * q_i < p_i, with p = e_query / K on each side (compared
-  // as u * e_q * K_t < e_t * K_d, both K > 0, to avoid divisions).
-  if (warp == 0) {
-    uint32_t st = 0;
-    int k = G;
-    for (int base = 0; base <= G; base += 32) {
-      const int i = base + lane;
-      bool rej = false;
-      if (i <= G) {
-        const RowStats t = ts[i];
-        st |= t.status;
-        if (i < G) {
-          const RowStats d = ds[i];
-          st |= d.status;
-          const int x = P.ids[static_cast<int64_t>(b) * G + i];
-          if (x < 0 || x >= V) st |= SV_ROW_BAD_DRAFT_ID;
-          const double u = static_cast<double>(P.u_accept[static_cast<int64_t>(b) * G + i]);
-          const double et = t.K > 0.0 ? static_cast<double>(t.e_query) : 0.0;
-          const double eq = d.K > 0.0 ? static_cast<double>(d.e_query) : 0.0;
-          const double kt = t.K > 0.0 ? t.K : 1.0, kd = d.K > 0.0 ? d.K : 1.0;
-          rej = !(u * eq * kt < et * kd);
-          if (seg == 0 && P.p_draft) P.p_draft[static_cast<int64_t>(b) * G + i] = static_cast<float>(et / kt);
-          if (seg == 0 && P.q_draft) P.q_draft[static_cast<int64_t>(b) * G + i] = static_cast<float>(eq / kd);
-        }
-      }
-      const unsigned m = __ballot_sync(0xffffffffu, rej);
-      if (m && k == G) k = base + __ffs(m) - 1;
-    }
-    st = __reduce_or_sync(0xffffffffu, st);
-    // The draw's two rows: target k and (when k < γ) draft k.
-    if (lane == 0) sh.pt = draw_side(ts[k]);
-    if (lane == 1 && k < G) sh.pd = draw_side(ds[k]);
-    if (lane == 0) {
-      sh.k = k;
-      sh.status = st;
-    }
+  // The batch row's decisions: made by the statistics pass (one thread
+  // fetches the record), or here by warp 0.
+  if (P.rec) {
+    if (tid < 3) reinterpret_cast<uint4*>(&sh.rec)[tid] = __ldcg(reinterpret_cast<const uint4*>(P.rec + b) + tid);
+  } else if (warp == 0) {
+    const DecideRecord r0 = decide_batch(P.dec, b);
+    if (lane == 0) sh.rec = r0;
   }
   __syncthreads();
-  const unsigned status = sh.status;
+  const DecideRecord rc = sh.rec;
+  const unsigned status = rc.status;
   int32_t* out = P.out_tokens + static_cast<int64_t>(b) * (G + 1);
   if (status & (SV_ROW_BAD_DRAFT_ID | SV_ROW_EMPTY)) {
     if (seg == 0) {
@@ -275,10 +238,10 @@ __global__ void __launch_bounds__(kDThreads, 2) decide_kernel(DecideParams P, in
     }
     return;
   }
-  const int k = sh.k;
+  const int k = rc.k;
   bool resid = k < G;
-  const DrawSide pt = sh.pt;
-  const DrawSide pd = resid ? sh.pd : DrawSide{0.0f, 0.0f, 0u, 0};
+  const DrawSide pt = rc.pt;
+  const DrawSide pd = rc.pd;
   RowView R;
   R.trow = static_cast<const ET*>(P.target) + (static_cast<int64_t>(b) * (G + 1) + k) * P.t_stride;
   R.drow = resid ? static_cast<const void*>(static_cast<const ED*>(P.draft) +

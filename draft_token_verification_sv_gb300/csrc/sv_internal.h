@@ -35,9 +35,10 @@ size_t topp_scratch_bytes(int rows0, int len0, int rows1, int len1);
 size_t decide_scratch_bytes(int B, int V);
 
 // Chain workspace: [counters: B u32][stats: B(2γ+1) RowStats][argmax: B(γ+1) i32]
-//                  [top-p scratch when T > 0 and top_p < 1][draw scratch when T > 0]
+//                  [decision records: B x 48 B][top-p scratch when T > 0 and
+//                  top_p < 1][draw scratch when T > 0]
 struct WorkspaceLayout {
-  size_t counters, stats, argmax, topp, decide, total;
+  size_t counters, stats, argmax, records, topp, decide, total;
 };
 
 inline WorkspaceLayout chain_workspace_layout(const sv_chain_desc& d) {
@@ -47,7 +48,8 @@ inline WorkspaceLayout chain_workspace_layout(const sv_chain_desc& d) {
   L.counters = 0;
   L.stats = align_up(B * sizeof(uint32_t), 256);
   L.argmax = L.stats + align_up(B * (2 * G + 1) * sizeof(RowStats), 256);
-  L.topp = L.argmax + align_up(B * (G + 1) * sizeof(int32_t), 256);
+  L.records = L.argmax + align_up(B * (G + 1) * sizeof(int32_t), 256);
+  L.topp = L.records + align_up(B * 48, 256);
   L.decide = L.topp;
   if (d.temperature > 0.0f && d.top_p < 1.0f)
     L.decide += align_up(topp_scratch_bytes(d.batch * (d.gamma + 1), d.vocab, d.batch * d.gamma, d.draft_vocab), 256);
@@ -57,13 +59,21 @@ inline WorkspaceLayout chain_workspace_layout(const sv_chain_desc& d) {
 }
 
 // Draft-side sampling / filtered probabilities:
-//   [stats: R RowStats][top-p scratch when top_p < 1][draw scratch]
+//   [stats: R RowStats][counters: R u32][decision records: R x 48 B]
+//   [top-p scratch when top_p < 1][draw scratch]
 inline size_t sample_stats_bytes(int rows) { return align_up(static_cast<size_t>(rows) * sizeof(RowStats), 256); }
+inline size_t sample_counters_offset(int rows) { return sample_stats_bytes(rows); }
+inline size_t sample_records_offset(int rows) {
+  return sample_counters_offset(rows) + align_up(static_cast<size_t>(rows) * sizeof(uint32_t), 256);
+}
+inline size_t sample_topp_offset(int rows) {
+  return sample_records_offset(rows) + align_up(static_cast<size_t>(rows) * 48, 256);
+}
 inline size_t sample_topp_bytes(const sv_sample_desc& d) {
   return d.temperature > 0.0f && d.top_p < 1.0f ? align_up(topp_scratch_bytes(d.rows, d.vocab, 0, 0), 256) : 0;
 }
 inline size_t sample_workspace_bytes(const sv_sample_desc& d) {
-  size_t n = sample_stats_bytes(d.rows) + sample_topp_bytes(d);
+  size_t n = sample_topp_offset(d.rows) + sample_topp_bytes(d);
   if (d.temperature > 0.0f) n += decide_scratch_bytes(d.rows, d.vocab);
   return n + 256;
 }

@@ -891,6 +891,17 @@ __global__ void __launch_bounds__(kSThreads, 3) topp_slice_kernel(StatsLaunch L)
     }
     S.out[r] = st;
   }
+  // Warp 0 alone (thread 0 wrote the statistics): count the row for its
+  // batch row and, after the batch row's last one, make its decisions.
+  if (L.dec.rec && warp == 0) {
+    bool last = false;
+    if (tid == 0) last = count_row(L.dec, S, r);
+    if (__shfl_sync(0xffffffffu, last, 0)) {
+      __threadfence();
+      const DecideRecord rc = decide_batch(L.dec, r / S.per_group);
+      if ((threadIdx.x & 31) == 0) L.dec.rec[r / S.per_group] = rc;
+    }
+  }
 }
 
 template <typename E>
