@@ -8,18 +8,20 @@
 // index (EAGLE3 draft rows: by target id).
 //
 // Work split, without clusters and without any block waiting for another:
-//  * slice blocks: every block reads one slice of 8192 logits of a row into
+//  * slice blocks: every block reads one slice of a row (8192 fp32 or 16384
+//    bf16 logits, eight 16-byte vectors per thread) into
 //    registers and takes the slice maximum.  Each logit falls in the
 //    ABSOLUTE eighth-octave bin f = floor(8 * l * c) (c = log2(e)/T), so that
 //    bins line up across the slices of a row.  The 256 bins below the slice
 //    maximum collect the logits' masses in fixed point relative to the bin's
-//    upper edge, v = round(2^21 * 2^(l*c - (f+1)/8)), summed exactly in
+//    upper edge, v = round(2^F * 2^(l*c - (f+1)/8)) (F = 21 for fp32, 20 for
+//    bf16 rows), summed exactly in
 //    per-warp u32 histograms (shared-memory integer reductions, no read-
 //    modify-write chains); lower logits add 2^(l*c - m_s*c) to a "far" sum.
 //    The block publishes (m_s, far, top bin, 256 bin sums) and bumps the row's
 //    counter;
 //  * the row's last slice block merges the summaries (a bin's mass is its
-//    summed v times 2^((f+1)/8 - 21 - m*c) whichever slice it came from),
+//    summed v times 2^((f+1)/8 - F - m*c) whichever slice it came from),
 //    finds the bin f* where the mass from the top first exceeds top_p * S,
 //    rescans the row (just read by its sibling blocks, so served by L2) to
 //    collect the logits of f* with their ids in shared memory, and resolves
@@ -33,8 +35,21 @@
 namespace sv {
 
 constexpr int kSThreads = 256;
-constexpr int kSEPT = 32;                       // logits per thread per slice
-constexpr int kSlice = kSThreads * kSEPT;       // logits per slice
+// Logits per thread per slice (eight 16-byte vectors either way) and the
+// fixed-point scale of the slice bins: a warp sums at most 32 * kEPT + 32
+// values below kFix, which stays under 2^32.
+template <typename E> struct SliceShape;
+template <> struct SliceShape<float> {
+  static constexpr int kEPT = 32;
+  static constexpr int kFixLog2 = 21;
+  static constexpr float kFix = 2097152.0f;  // 2^21
+};
+template <> struct SliceShape<uint16_t> {
+  static constexpr int kEPT = 64;
+  static constexpr int kFixLog2 = 20;
+  static constexpr float kFix = 1048576.0f;  // 2^20
+};
+constexpr int kMinSlice = kSThreads * 32;       // the smaller slice (scratch sizing)
 constexpr int kNB = 256;                        // eighth-octave bins under a slice maximum
 constexpr int kSummary = 4 + kNB;               // floats per slice summary
 constexpr int kCandCap = 4096;                  // candidates of the cut bin in shared memory
@@ -42,7 +57,6 @@ constexpr int kFinal = 64;
 constexpr int kMaxStaged = kCandCap / 2;         // slice headers staged in shared memory
 constexpr int kRegion = kCandCap / (kSThreads / 32);  // candidates per warp in the rescan
 constexpr int kWarps = kSThreads / 32;
-constexpr float kFixBin = 2097152.0f;           // 2^21: slice bin masses, units of the bin's upper edge
 constexpr float kFixCand = 524288.0f;           // 2^19: candidate level masses
 constexpr double kScale40 = 1099511627776.0;    // generic path: masses in units of 2^-40
 constexpr double kInv40 = 1.0 / 1099511627776.0;
@@ -593,7 +607,7 @@ __device__ void resolve_candidates(ToppShared& sh, const RowSet& S, float c, flo
 template <typename E>
 __global__ void __launch_bounds__(kSThreads, 3) topp_slice_kernel(StatsLaunch L) {
   constexpr int EPV = Elem<E>::kPerVec;
-  constexpr int VPT = kSEPT / EPV;          // 16-byte vectors per thread
+  constexpr int VPT = SliceShape<E>::kEPT / EPV;  // 16-byte vectors per thread
   constexpr int VPS = VPT * kSThreads;      // vectors per slice
   extern __shared__ __align__(16) unsigned char dyn_smem[];
   ToppShared& sh = *reinterpret_cast<ToppShared*>(dyn_smem);
@@ -657,7 +671,7 @@ __global__ void __launch_bounds__(kSThreads, 3) topp_slice_kernel(StatsLaunch L)
     if (fy > lowf) {
       // l*c - (f+1)/8 in [-1/8, 0]: the mass relative to the bin's upper edge.
       const float t = fmaf(x, c, fmaf(fy, -0.125f, -0.125f));
-      atomicAdd(&wh[static_cast<int>(Gsf - fy)], __float2uint_rn(ex2v(t) * kFixBin));
+      atomicAdd(&wh[static_cast<int>(Gsf - fy)], __float2uint_rn(ex2v(t) * SliceShape<E>::kFix));
     } else {
       far += ex2v(fmaf(x, c, -mcs));
     }
@@ -705,6 +719,7 @@ __global__ void __launch_bounds__(kSThreads, 3) topp_slice_kernel(StatsLaunch L)
   double K = 0.0;
   if (!empty) {
     const float Grf = floorf(m * c8);
+    constexpr float kFixL2 = static_cast<float>(SliceShape<E>::kFixLog2);
     unsigned long long acc = 0;
     float farp = 0.0f;
     if (ns <= kMaxStaged) {
@@ -739,7 +754,7 @@ __global__ void __launch_bounds__(kSThreads, 3) topp_slice_kernel(StatsLaunch L)
         for (int u = 0; u < 8; ++u) {
           acc += static_cast<unsigned long long>(v[u]);
           if (w[u] > 0.0f)
-            farp += w[u] * ex2v((hg[q0 + u] - static_cast<float>(tid) + 1.0f) * 0.125f - mc - 21.0f);
+            farp += w[u] * ex2v((hg[q0 + u] - static_cast<float>(tid) + 1.0f) * 0.125f - mc - kFixL2);
         }
       }
     } else {
@@ -752,17 +767,18 @@ __global__ void __launch_bounds__(kSThreads, 3) topp_slice_kernel(StatsLaunch L)
         const int D = static_cast<int>(Grf - Gq);
         if (tid >= D && tid < kNB) acc += static_cast<unsigned long long>(__ldcg(sq + 4 + (tid - D)));
         if (tid >= kNB - D && tid < kNB)
-          farp += __ldcg(sq + 4 + tid) * ex2v((Gq - static_cast<float>(tid) + 1.0f) * 0.125f - mc - 21.0f);
+          farp += __ldcg(sq + 4 + tid) * ex2v((Gq - static_cast<float>(tid) + 1.0f) * 0.125f - mc - kFixL2);
         if (tid == 0) farp += __ldcg(sq + 1) * ex2v(fmaf(mq, c, -mc));
       }
     }
-    // Mass of one unit of bin Gr - b: 2^((Gr - b + 1)/8 - 21 - mc), with the
+    // Mass of one unit of bin Gr - b: 2^((Gr - b + 1)/8 - kFixLog2 - mc), with the
     // exponent split into whole and eighth powers of two.
     if (tid == 0) sh.unit = static_cast<double>(ex2v(floorf(mc) - mc));
     __syncthreads();
     const int kb = static_cast<int>(Grf) - tid + 1;
     const int kq = kb >> 3, kr = kb & 7;
-    const double scale = pow2i(kq - static_cast<int>(floorf(mc)) - 21) * pow2_eighths(kr) * sh.unit;
+    const double scale =
+        pow2i(kq - static_cast<int>(floorf(mc)) - SliceShape<E>::kFixLog2) * pow2_eighths(kr) * sh.unit;
     const double mass = static_cast<double>(acc) * scale;
     double tot;
     const double excl = block_exclusive_scan_d<kSThreads>(mass, sh.scan, &tot);
@@ -774,7 +790,7 @@ __global__ void __launch_bounds__(kSThreads, 3) topp_slice_kernel(StatsLaunch L)
     if (mass > 0.0 && excl <= limit && excl + mass > limit) {
       sh.gstar = tid;
       sh.above0 = excl;
-      sh.unit = scale * 4.0;  // candidate masses are in units of 2^-19 of the bin's edge
+      sh.unit = scale * pow2i(SliceShape<E>::kFixLog2 - 19);  // candidate masses: units of 2^-19 of the bin's edge
     }
     __syncthreads();
     const int gstar = sh.gstar;
@@ -920,7 +936,8 @@ static sv_status launch_typed(const StatsLaunch& L, cudaStream_t stream) {
   return SV_OK;
 }
 
-int topp_slices(int len) { return len <= 0 ? 1 : (len + kSlice - 1) / kSlice; }
+static int slices_of(int len, int slice) { return len <= 0 ? 1 : (len + slice - 1) / slice; }
+int topp_slices(int len) { return slices_of(len, kMinSlice); }
 
 size_t topp_scratch_bytes(int rows0, int len0, int rows1, int len1) {
   const size_t slices = static_cast<size_t>(rows0) * topp_slices(len0) + static_cast<size_t>(rows1) * topp_slices(len1);
@@ -932,7 +949,8 @@ size_t topp_scratch_bytes(int rows0, int len0, int rows1, int len1) {
 sv_status launch_topp_stats(StatsLaunch L, sv_dtype dtype, void* scratch, cudaStream_t stream) {
   const int rows = L.set[0].rows + (L.nsets > 1 ? L.set[1].rows : 0);
   if (rows == 0) return SV_OK;
-  for (int i = 0; i < L.nsets; ++i) L.nslices[i] = topp_slices(L.set[i].len);
+  const int slice = kSThreads * (dtype == SV_BF16 ? SliceShape<uint16_t>::kEPT : SliceShape<float>::kEPT);
+  for (int i = 0; i < L.nsets; ++i) L.nslices[i] = slices_of(L.set[i].len, slice);
   const size_t slices = static_cast<size_t>(L.set[0].rows) * L.nslices[0] +
                         (L.nsets > 1 ? static_cast<size_t>(L.set[1].rows) * L.nslices[1] : 0);
   L.summ = static_cast<float*>(scratch);
