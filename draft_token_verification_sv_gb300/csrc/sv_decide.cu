@@ -207,7 +207,7 @@ __device__ __forceinline__ float block_sum_to0(float v, DecideShared& sh) {
 }
 
 template <typename ET, typename ED, int NC>
-__global__ void __launch_bounds__(kDThreads, 2) decide_kernel(DecideParams P, int nseg) {
+__global__ void __launch_bounds__(kDThreads, NC >= 8 ? 2 : 3) decide_kernel(DecideParams P, int nseg) {
   __shared__ DecideShared sh;
   const int b = blockIdx.x / nseg;
   const int seg = blockIdx.x - b * nseg;
@@ -463,7 +463,7 @@ static int chunks_per_block(int B, int V, int nc_max) {
 sv_status launch_decide(const DecideParams& P, sv_dtype td, sv_dtype dd, void* scratch, cudaStream_t stream) {
   if (P.B == 0) return SV_OK;
   const bool tb = td == SV_BF16, db = dd == SV_BF16;
-  const int nc = chunks_per_block(P.B, P.V, tb && db && !P.t2d ? 8 : 4);
+  const int nc = chunks_per_block(P.B, P.V, 4);
   if (tb && db) {
     if (nc == 8) return launch_decide_typed<uint16_t, uint16_t, 8>(P, scratch, stream);
     if (nc == 4) return launch_decide_typed<uint16_t, uint16_t, 4>(P, scratch, stream);
