@@ -17,9 +17,8 @@
 //    upper edge, v = round(2^F * 2^(l*c - (f+1)/8)) (F = 21 for fp32, 20 for
 //    bf16 rows), summed exactly in
 //    per-warp u32 histograms (shared-memory integer reductions, no read-
-//    modify-write chains); lower logits add 2^(l*c - m_s*c) to a "far" sum.
-//    The block publishes (m_s, far, top bin, 256 bin sums) and bumps the row's
-//    counter;
+//    modify-write chains); lower logits count in the lowest bin.  The block
+//    publishes (m_s, top bin, 256 bin sums) and bumps the row's counter;
 //  * the row's last slice block merges the summaries (a bin's mass is its
 //    summed v times 2^((f+1)/8 - F - m*c) whichever slice it came from),
 //    finds the bin f* where the mass from the top first exceeds top_p * S,
@@ -28,9 +27,12 @@
 //    the cut among them by radix levels over their order keys, ending with
 //    an exact sort of the last <= 64 by (logit descending, tie key ascending)
 //    walked in double precision.
-// Rare rows (the cut below the 32 octaves under the maximum, more than 4096
-// logits in f*) take an exact radix select over the order keys of the row.
+// Rare rows (the cut in the lowest of the 256 bins under the maximum or
+// below, more than 4096 logits in f*) take an exact radix select over the
+// order keys of the row.
 #include "sv_rows.cuh"
+
+#include <cuda_bf16.h>
 
 namespace sv {
 
@@ -91,6 +93,13 @@ struct ToppShared {
   double above0, limit, total, kept_mass, unit;
   float xlo, xhi;
 };
+
+// Two bf16 logits in one 32-bit word.
+__device__ __forceinline__ __nv_bfloat162 bf2_of(uint32_t w) {
+  __nv_bfloat162 r;
+  memcpy(&r, &w, sizeof(r));
+  return r;
+}
 
 // exp2 that the compiler may not merge with an identical earlier one.
 __device__ __forceinline__ float ex2v(float x) {
@@ -652,29 +661,40 @@ __global__ void __launch_bounds__(kSThreads, 3) topp_slice_kernel(StatsLaunch L)
     if (xi >= 0) xv = Elem<E>::load(row + xi);
   }
   float lm = xv;
+  if constexpr (sizeof(E) == 2) {
+    // Packed bf16 maxima, two logits per instruction.
+    __nv_bfloat162 m2 = bf2_of(0xff80ff80u);
 #pragma unroll
-  for (int k = 0; k < VPT; ++k)
+    for (int k = 0; k < VPT; ++k) {
+      m2 = __hmax2(m2, bf2_of(raw[k].x));
+      m2 = __hmax2(m2, bf2_of(raw[k].y));
+      m2 = __hmax2(m2, bf2_of(raw[k].z));
+      m2 = __hmax2(m2, bf2_of(raw[k].w));
+    }
+    lm = fmaxf(lm, fmaxf(__low2float(m2), __high2float(m2)));
+  } else {
 #pragma unroll
-    for (int i = 0; i < EPV; ++i) lm = fmaxf(lm, Elem<E>::at(raw[k], i));
+    for (int k = 0; k < VPT; ++k)
+#pragma unroll
+      for (int i = 0; i < EPV; ++i) lm = fmaxf(lm, Elem<E>::at(raw[k], i));
+  }
   const float ms = block_max<kSThreads>(lm, sh.red_f);
 
-  // 2. Bin sums over the 256 eighth-octaves under the slice maximum; the
-  // rest adds 2^(l*c - m_s*c) to `far`.
+  // 2. Bin sums over the 256 eighth-octaves under the slice maximum.  Lower
+  // logits are counted in the lowest bin with their mass relative to its
+  // edge (they round to 0 more than 21 octaves below it, and are skipped);
+  // the merge never resolves a cut inside that bin (exact path instead).
   const bool live = ms > -CUDART_INF_F;
   const float Gsf = live ? floorf(ms * c8) : 0.0f;
-  const float lowf = Gsf - static_cast<float>(kNB);
-  const float mcs = ms * c;
-  float far = 0.0f;
+  const float bottom = Gsf - static_cast<float>(kNB - 1);
   unsigned* wh = sh.wh[warp];
   auto add = [&](float x) {
-    const float fy = floorf(x * c8);
-    if (fy > lowf) {
-      // l*c - (f+1)/8 in [-1/8, 0]: the mass relative to the bin's upper edge.
-      const float t = fmaf(x, c, fmaf(fy, -0.125f, -0.125f));
-      atomicAdd(&wh[static_cast<int>(Gsf - fy)], __float2uint_rn(ex2v(t) * SliceShape<E>::kFix));
-    } else {
-      far += ex2v(fmaf(x, c, -mcs));
-    }
+    const float fy = fmaxf(floorf(x * c8), bottom);
+    // l*c - (f+1)/8 (in [-1/8, 0] inside the window): the mass relative to
+    // the bin's upper edge.
+    const float t = fmaf(x, c, fmaf(fy, -0.125f, -0.125f));
+    const unsigned v = __float2uint_rn(ex2v(t) * SliceShape<E>::kFix);
+    if (v) atomicAdd(&wh[static_cast<int>(Gsf - fy)], v);
   };
   if (live) {
 #pragma unroll
@@ -692,10 +712,9 @@ __global__ void __launch_bounds__(kSThreads, 3) topp_slice_kernel(StatsLaunch L)
     for (int w = 0; w < kWarps; ++w) a += sh.wh[w][tid];
     out[4 + tid] = static_cast<float>(a);
   }
-  far = block_sum<kSThreads>(far, sh.red_f);
   if (tid == 0) {
     out[0] = ms;
-    out[1] = far;
+    out[1] = 0.0f;  // no mass outside the bins
     out[2] = Gsf;
     out[3] = 0.0f;
   }
@@ -801,6 +820,8 @@ __global__ void __launch_bounds__(kSThreads, 3) topp_slice_kernel(StatsLaunch L)
       // cut lies among the masses below them (exact path).
       generic = limit < Z;
       if (!generic) K = Z;
+    } else if (gstar == kNB - 1) {
+      generic = true;  // the lowest bin also holds the logits below the window
     } else {
       // Rescan: the logits of the cut bin with their ids, each warp into its
       // own region of the list; if a region overflows, again with one
