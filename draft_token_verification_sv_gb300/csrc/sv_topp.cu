@@ -94,6 +94,27 @@ struct ToppShared {
   float xlo, xhi;
 };
 
+// L2 eviction priorities: the slice pass marks a row's lines evict-last so
+// they survive until the row's last block rescans them; the rescan marks
+// them evict-first once used.  Hints only: results do not depend on them.
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint4 ldg_hint(const uint4* a, uint64_t pol) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(a), "l"(pol));
+  return r;
+}
+
 // Two bf16 logits in one 32-bit word.
 __device__ __forceinline__ __nv_bfloat162 bf2_of(uint32_t w) {
   __nv_bfloat162 r;
@@ -180,11 +201,12 @@ __device__ __forceinline__ void scan_row(const E* row, int len, F&& f) {
   const RowSplit rs = split_row(row, len);
   const uint4* vp = reinterpret_cast<const uint4*>(row + rs.head);
   const int v0 = static_cast<int>(threadIdx.x);
+  const uint64_t drop = l2_policy_evict_first();
   auto load = [&](uint4* w, int base) {
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int v = base + v0 + u * kSThreads;
-      w[u] = v < rs.nvec ? __ldcg(vp + v) : Elem<E>::neg_inf_vec();
+      w[u] = v < rs.nvec ? ldg_hint(vp + v, drop) : Elem<E>::neg_inf_vec();
     }
   };
   auto use = [&](const uint4* w, int base) {
@@ -642,15 +664,16 @@ __global__ void __launch_bounds__(kSThreads, 3) topp_slice_kernel(StatsLaunch L)
 #pragma unroll
   for (int i = 0; i < kWarps * kNB / kSThreads; ++i) (&sh.wh[0][0])[i * kSThreads + tid] = 0u;
 
-  // 1. The slice in registers; slice maximum.  Normal L2 policy (not the
-  // streaming evict-first one): the row's last block rescans it from L2.
+  // 1. The slice in registers; slice maximum.  Evict-last in L2: the row's
+  // last block rescans it from L2.
   const RowSplit rs = split_row(row, S.len);
   const uint4* vp = reinterpret_cast<const uint4*>(row + rs.head);
+  const uint64_t keep = l2_policy_evict_last();
   uint4 raw[VPT];
 #pragma unroll
   for (int k = 0; k < VPT; ++k) {
     const int v = s * VPS + k * kSThreads + tid;
-    raw[k] = v < rs.nvec ? __ldcg(vp + v) : Elem<E>::neg_inf_vec();
+    raw[k] = v < rs.nvec ? ldg_hint(vp + v, keep) : Elem<E>::neg_inf_vec();
   }
   float xv = -CUDART_INF_F;
   if (s == 0) {
