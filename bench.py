@@ -457,8 +457,9 @@ def run_ours(args, dist: Dist):
 
 
 def config_of(cfg, workload, nsets, world):
-    c = {"workload": workload, "batch": cfg.batch, "vocab": cfg.vocab, "dtype": cfg.dtype,
-         "l2": f"{nsets} rotating input copies ({nsets * step_bytes(cfg) / 1e6:.0f} MB > 4x L2)",
+    l2 = f"{nsets} rotating input copies ({nsets * step_bytes(cfg) / 1e6:.0f} MB > 4x L2)" if nsets else \
+        "not applicable (CPU oracle)"
+    c = {"workload": workload, "batch": cfg.batch, "vocab": cfg.vocab, "dtype": cfg.dtype, "l2": l2,
          "parallelism": f"replicas x{world} (batch rows independent)"}
     if isinstance(cfg, synth.TreeConfig):
         c.update(nodes=cfg.nodes, max_depth=cfg.max_depth, temperature=0.0)
@@ -587,7 +588,7 @@ def run_reference(args, dist: Dist):
     return {"impl": "reference", "metric": "verify rows/s (B*(2*gamma+1) rows per chain step, B*N per tree step)",
             "value": value, "unit": "rows/s", "n_gpus": dist.world, "steps": K, "warmup": W,
             "ms_per_step": 1e3 * total / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "f64", "data": "synthetic (seeded)", "config": config_of(cfg, args.workload, 1, 1),
+            "dtype": "f64", "data": "synthetic (seeded)", "config": config_of(cfg, args.workload, 0, 1),
             "cpu_baseline": {"value": value, "unit": "rows/s", "cores": 1, "kind": "oracle",
                              "sample": f"{per_step} batch rows of the {cfg.name} workload per step"},
             "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
