@@ -218,13 +218,15 @@ __device__ __forceinline__ void scan_row(const E* row, int len, F&& f) {
     }
   };
   uint4 a[U], b[U];
+#pragma unroll
+  for (int u = 0; u < U; ++u) b[u] = Elem<E>::neg_inf_vec();
   if (rs.nvec > 0) load(a, 0);
-  for (int base = 0; base < rs.nvec; base += 2 * kStep) {
+  // One copy of the loop body: the next batch lands in b, then moves to a.
+  for (int base = 0; base < rs.nvec; base += kStep) {
     if (base + kStep < rs.nvec) load(b, base + kStep);
     use(a, base);
-    if (base + kStep >= rs.nvec) break;
-    if (base + 2 * kStep < rs.nvec) load(a, base + 2 * kStep);
-    use(b, base + kStep);
+#pragma unroll
+    for (int u = 0; u < U; ++u) a[u] = b[u];
   }
   const int ntail = len - rs.tail0;
   for (int t0 = 0; t0 < rs.head + ntail; t0 += kSThreads) {
@@ -711,19 +713,21 @@ __global__ void __launch_bounds__(kSThreads, 3) topp_slice_kernel(StatsLaunch L)
   const float Gsf = live ? floorf(ms * c8) : 0.0f;
   const float bottom = Gsf - static_cast<float>(kNB - 1);
   unsigned* wh = sh.wh[warp];
+  // Plain (reorderable) exp2 and widening here, so the per-logit chains of
+  // different logits interleave around the shared-memory reductions.
   auto add = [&](float x) {
     const float fy = fmaxf(floorf(x * c8), bottom);
     // l*c - (f+1)/8 (in [-1/8, 0] inside the window): the mass relative to
     // the bin's upper edge.
     const float t = fmaf(x, c, fmaf(fy, -0.125f, -0.125f));
-    const unsigned v = __float2uint_rn(ex2v(t) * SliceShape<E>::kFix);
+    const unsigned v = __float2uint_rn(ex2(t) * SliceShape<E>::kFix);
     if (v) atomicAdd(&wh[static_cast<int>(Gsf - fy)], v);
   };
   if (live) {
 #pragma unroll
     for (int k = 0; k < VPT; ++k)
 #pragma unroll
-      for (int i = 0; i < EPV; ++i) add(widen<E>(raw[k], i));
+      for (int i = 0; i < EPV; ++i) add(Elem<E>::at(raw[k], i));
     if (xv > -CUDART_INF_F) add(xv);
   }
   __syncthreads();
@@ -751,9 +755,21 @@ __global__ void __launch_bounds__(kSThreads, 3) topp_slice_kernel(StatsLaunch L)
   // 3. Last slice block of the row: merge the summaries.  Thread b owns the
   // row bin Gr - b; slice bins below the row's 256 go to `far`.
   const float* sum0 = L.summ + static_cast<int64_t>(sbase) * kSummary;
+  // Slice maxima and top bins, staged in shared memory when they fit.
+  const bool staged = ns <= kMaxStaged;
+  float* hm = sh.cand.x;               // slice maximum
+  float* hg = sh.cand.x + kMaxStaged;  // slice top bin
   float m = -CUDART_INF_F;
-  for (int q = tid; q < ns; q += kSThreads) m = fmaxf(m, __ldcg(sum0 + static_cast<int64_t>(q) * kSummary));
-  m = block_max<kSThreads>(m, sh.red_f);
+  for (int q = tid; q < ns; q += kSThreads) {
+    const float* sq = sum0 + static_cast<int64_t>(q) * kSummary;
+    const float mq = __ldcg(sq);
+    m = fmaxf(m, mq);
+    if (staged) {
+      hm[q] = mq;
+      hg[q] = __ldcg(sq + 2);
+    }
+  }
+  m = block_max<kSThreads>(m, sh.red_f);  // its barriers also publish the staging
   const bool empty = !(m > -CUDART_INF_F);
   const float mc = m * c;
   uint32_t tau = 0u;
@@ -763,34 +779,21 @@ __global__ void __launch_bounds__(kSThreads, 3) topp_slice_kernel(StatsLaunch L)
     const float Grf = floorf(m * c8);
     constexpr float kFixL2 = static_cast<float>(SliceShape<E>::kFixLog2);
     unsigned long long acc = 0;
-    float farp = 0.0f;
-    if (ns <= kMaxStaged) {
-      // Slice headers staged in shared memory, then every bin load of every
-      // slice issued independently.
-      float* hg = sh.cand.x;                          // slice top bin
-      int* hd = sh.cand.j;                            // row top bin - slice top bin (huge: empty)
-      for (int q = tid; q < ns; q += kSThreads) {
-        const float* sq = sum0 + static_cast<int64_t>(q) * kSummary;
-        const float mq = __ldcg(sq);
-        const float Gq = __ldcg(sq + 2);
-        const bool lq = mq > -CUDART_INF_F;
-        hg[q] = Gq;
-        hd[q] = lq ? static_cast<int>(Grf - Gq) : (1 << 24);
-        if (lq) farp += __ldcg(sq + 1) * ex2v(fmaf(mq, c, -mc));
-      }
-      __syncthreads();
-      // Eight slices at a time, every load issued before any is used.
+    float farp = 0.0f;  // slice bins below the row's 256 bins
+    if (staged) {
+      // Eight slices at a time, every bin load issued before any is used.
 #pragma unroll 1
       for (int q0 = 0; q0 < ns; q0 += 8) {
         float v[8], w[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
           const int q = q0 + u;
-          const int D = q < ns ? hd[q] : (1 << 24);
-          const float* sq = sum0 + static_cast<int64_t>(q < ns ? q : 0) * kSummary + 4;
+          const bool lq = q < ns && hm[q] > -CUDART_INF_F;
+          const int D = lq ? static_cast<int>(Grf - hg[q]) : (1 << 24);
+          const float* sq = sum0 + static_cast<int64_t>(lq ? q : 0) * kSummary + 4;
           v[u] = (tid >= D && tid < kNB) ? __ldcg(sq + (tid - D)) : 0.0f;
           // Slice bin Gq - tid lies below the row's bins.
-          w[u] = (D < (1 << 24) && tid >= kNB - D && tid < kNB) ? __ldcg(sq + tid) : 0.0f;
+          w[u] = (lq && tid >= kNB - D && tid < kNB) ? __ldcg(sq + tid) : 0.0f;
         }
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
@@ -810,17 +813,15 @@ __global__ void __launch_bounds__(kSThreads, 3) topp_slice_kernel(StatsLaunch L)
         if (tid >= D && tid < kNB) acc += static_cast<unsigned long long>(__ldcg(sq + 4 + (tid - D)));
         if (tid >= kNB - D && tid < kNB)
           farp += __ldcg(sq + 4 + tid) * ex2v((Gq - static_cast<float>(tid) + 1.0f) * 0.125f - mc - kFixL2);
-        if (tid == 0) farp += __ldcg(sq + 1) * ex2v(fmaf(mq, c, -mc));
       }
     }
     // Mass of one unit of bin Gr - b: 2^((Gr - b + 1)/8 - kFixLog2 - mc), with the
     // exponent split into whole and eighth powers of two.
-    if (tid == 0) sh.unit = static_cast<double>(ex2v(floorf(mc) - mc));
-    __syncthreads();
+    const double frac_unit = static_cast<double>(ex2(floorf(mc) - mc));
     const int kb = static_cast<int>(Grf) - tid + 1;
     const int kq = kb >> 3, kr = kb & 7;
     const double scale =
-        pow2i(kq - static_cast<int>(floorf(mc)) - SliceShape<E>::kFixLog2) * pow2_eighths(kr) * sh.unit;
+        pow2i(kq - static_cast<int>(floorf(mc)) - SliceShape<E>::kFixLog2) * pow2_eighths(kr) * frac_unit;
     const double mass = static_cast<double>(acc) * scale;
     double tot;
     const double excl = block_exclusive_scan_d<kSThreads>(mass, sh.scan, &tot);
