@@ -638,7 +638,7 @@ __device__ void resolve_candidates(ToppShared& sh, const RowSet& S, float c, flo
 }
 
 template <typename E>
-__global__ void __launch_bounds__(kSThreads, 3) topp_slice_kernel(StatsLaunch L) {
+__global__ void __launch_bounds__(kSThreads, 5) topp_slice_kernel(StatsLaunch L) {
   constexpr int EPV = Elem<E>::kPerVec;
   constexpr int VPT = SliceShape<E>::kEPT / EPV;  // 16-byte vectors per thread
   constexpr int VPS = VPT * kSThreads;      // vectors per slice
