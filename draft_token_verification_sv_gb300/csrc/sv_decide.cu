@@ -207,7 +207,7 @@ __device__ __forceinline__ float block_sum_to0(float v, DecideShared& sh) {
 }
 
 template <typename ET, typename ED, int NC>
-__global__ void __launch_bounds__(kDThreads, NC >= 8 ? 2 : 3) decide_kernel(DecideParams P, int nseg) {
+__global__ void __launch_bounds__(kDThreads, NC >= 8 ? 2 : 4) decide_kernel(DecideParams P, int nseg) {
   __shared__ DecideShared sh;
   const int b = blockIdx.x / nseg;
   const int seg = blockIdx.x - b * nseg;
