@@ -447,6 +447,78 @@ __device__ __noinline__ void generic_select(ToppShared& sh, const E* row, const 
   K_out = static_cast<double>(above + nk * e_tau) * kInv40;
 }
 
+// Ids of the logits in [xlo, xhi) into this warp's region of sh.cand.j:
+// per batch of 16-byte vectors each thread builds a bit mask of its
+// candidates, then the warp drains the set bits with ballots (the values
+// are fetched afterwards).  Returns the warp's count, which may exceed the
+// region (entries past it are dropped).  Block-uniform trip counts.
+template <typename E>
+__device__ __forceinline__ int collect_ids(ToppShared& sh, const E* row, int len, float xlo, float xhi) {
+  constexpr int EPV = Elem<E>::kPerVec;
+  constexpr int U = 4;
+  constexpr int kStep = kSThreads * U;
+  static_assert(U * EPV <= 32, "one mask bit per logit of a batch");
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const unsigned lane_lt = (1u << lane) - 1u;
+  int* region = sh.cand.j + warp * kRegion;
+  const RowSplit rs = split_row(row, len);
+  const uint4* vp = reinterpret_cast<const uint4*>(row + rs.head);
+  const uint64_t drop = l2_policy_evict_first();
+  const int v0 = static_cast<int>(threadIdx.x);
+  int wn = 0;
+  auto load = [&](uint4* w, int base) {
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int v = base + v0 + u * kSThreads;
+      w[u] = v < rs.nvec ? ldg_hint(vp + v, drop) : Elem<E>::neg_inf_vec();
+    }
+  };
+  auto use = [&](const uint4* w, int base) {
+    unsigned mask = 0;
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+#pragma unroll
+      for (int i = 0; i < EPV; ++i) {
+        const float x = Elem<E>::at(w[u], i);
+        if (x >= xlo && x < xhi) mask |= 1u << (u * EPV + i);
+      }
+    while (__ballot_sync(0xffffffffu, mask != 0)) {
+      const bool has = mask != 0;
+      const unsigned bal = __ballot_sync(0xffffffffu, has);
+      if (has) {
+        const int bit = __ffs(mask) - 1;
+        const int u = bit / EPV, i = bit - u * EPV;
+        const int slot = wn + __popc(bal & lane_lt);
+        if (slot < kRegion) region[slot] = rs.head + (base + v0 + u * kSThreads) * EPV + i;
+        mask &= mask - 1;
+      }
+      wn += __popc(bal);
+    }
+  };
+  uint4 a[U], b[U];
+#pragma unroll
+  for (int u = 0; u < U; ++u) b[u] = Elem<E>::neg_inf_vec();
+  if (rs.nvec > 0) load(a, 0);
+  for (int base = 0; base < rs.nvec; base += kStep) {
+    if (base + kStep < rs.nvec) load(b, base + kStep);
+    use(a, base);
+#pragma unroll
+    for (int u = 0; u < U; ++u) a[u] = b[u];
+  }
+  const int ntail = len - rs.tail0;
+  for (int t0 = 0; t0 < rs.head + ntail; t0 += kSThreads) {
+    const int t = t0 + static_cast<int>(threadIdx.x);
+    const int j = t < rs.head ? t : (t < rs.head + ntail ? rs.tail0 + (t - rs.head) : -1);
+    const float x = j >= 0 ? Elem<E>::load(row + j) : -CUDART_INF_F;
+    const bool cand = x >= xlo && x < xhi;
+    const unsigned bal = __ballot_sync(0xffffffffu, cand);
+    const int slot = wn + __popc(bal & lane_lt);
+    if (cand && slot < kRegion) region[slot] = j;
+    wn += __popc(bal);
+  }
+  return wn;
+}
+
 // The cut among the candidates of the cut bin (n <= kCandCap, in
 // sh.cand): radix levels over their order keys, each keeping the digit where
 // the mass from the top first exceeds the limit (counts and fixed-point
@@ -859,19 +931,7 @@ __global__ void __launch_bounds__(kSThreads, 5) topp_slice_kernel(StatsLaunch L)
       }
       __syncthreads();
       const float xlo = sh.xlo, xhi = sh.xhi;
-      int wn = 0;
-      scan_row<E>(row, S.len, [&](float x, int j) {
-        const bool cand = x >= xlo && x < xhi;
-        const unsigned bal = __ballot_sync(0xffffffffu, cand);
-        if (bal) {
-          const int slot = wn + __popc(bal & lane_lt);
-          if (cand && slot < kRegion) {
-            sh.cand.x[warp * kRegion + slot] = x;
-            sh.cand.j[warp * kRegion + slot] = j;
-          }
-          wn += __popc(bal);
-        }
-      });
+      const int wn = collect_ids<E>(sh, row, S.len, xlo, xhi);
       if (lane == 0) sh.wcnt[warp] = wn;
       __syncthreads();
       int total_c = 0, my_off = 0, over = 0;
@@ -886,22 +946,17 @@ __global__ void __launch_bounds__(kSThreads, 5) topp_slice_kernel(StatsLaunch L)
         // Pack the regions to the front in warp order: every entry is read
         // into registers before any is written.
         constexpr int kPer = kRegion / 32;
-        float rx[kPer];
         int rj[kPer];
 #pragma unroll
         for (int k = 0; k < kPer; ++k) {
           const int e2 = lane + 32 * k;
-          rx[k] = e2 < wn ? sh.cand.x[warp * kRegion + e2] : 0.0f;
           rj[k] = e2 < wn ? sh.cand.j[warp * kRegion + e2] : 0;
         }
         __syncthreads();
 #pragma unroll
         for (int k = 0; k < kPer; ++k) {
           const int e2 = lane + 32 * k;
-          if (e2 < wn) {
-            sh.cand.x[my_off + e2] = rx[k];
-            sh.cand.j[my_off + e2] = rj[k];
-          }
+          if (e2 < wn) sh.cand.j[my_off + e2] = rj[k];
         }
         if (tid == 0) sh.ncand = total_c;
       } else if (total_c <= kCandCap) {
@@ -927,6 +982,11 @@ __global__ void __launch_bounds__(kSThreads, 5) topp_slice_kernel(StatsLaunch L)
       __syncthreads();
       const int n = sh.ncand;
       generic = n == 0 || n > kCandCap;
+      if (!generic) {
+        // The candidates' logits: one parallel round of loads (served by L2).
+        for (int i = tid; i < n; i += kSThreads) sh.cand.x[i] = load_at<E>(row, sh.cand.j[i]);
+        __syncthreads();
+      }
       if (!generic)
         resolve_candidates<E>(sh, S, c, mc, n, -(Bf + 1.0f) * 0.125f, above0, limit, unit, tau, cut, K);
     }
