@@ -265,7 +265,7 @@ __global__ void __launch_bounds__(THREADS) greedy_kernel(GreedyParams P) {
 template <typename E, GreedyMode MODE>
 static sv_status launch_greedy(const GreedyParams& P, int rows, cudaStream_t stream) {
   constexpr int kThreads = 512;
-  constexpr int kUnroll = 4;
+  constexpr int kUnroll = 8;
   if (rows == 0) return SV_OK;
   greedy_kernel<E, kThreads, kUnroll, MODE><<<rows, kThreads, 0, stream>>>(P);
   if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
