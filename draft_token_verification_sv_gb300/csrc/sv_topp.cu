@@ -129,20 +129,6 @@ __device__ __forceinline__ float ex2v(float x) {
   return y;
 }
 
-template <typename E>
-__device__ __forceinline__ float widen(const uint4& v, int i) {
-  if constexpr (sizeof(E) == 4) {
-    return Elem<E>::at(v, i);
-  } else {
-    // Volatile so that every pass widens again instead of keeping 2x data live.
-    const uint32_t w = (i >> 1) == 0 ? v.x : (i >> 1) == 1 ? v.y : (i >> 1) == 2 ? v.z : v.w;
-    uint32_t r;
-    if (i & 1) asm volatile("and.b32 %0, %1, 0xffff0000;" : "=r"(r) : "r"(w));
-    else asm volatile("shl.b32 %0, %1, 16;" : "=r"(r) : "r"(w));
-    return __uint_as_float(r);
-  }
-}
-
 // 2^n for an integer n in the normal double range.
 __device__ __forceinline__ double pow2i(int n) {
   return __longlong_as_double(static_cast<long long>(n + 1023) << 52);
