@@ -48,7 +48,11 @@ WORKLOADS = {
     "llama3-sample": synth.LLAMA3_SAMPLE,
     "qwen3-d2t": synth.QWEN3_D2T,
     "tree": synth.TREE,
+    "tree-path": synth.TREE,
 }
+# Workloads verified by the path walk (sv_verify_tree_path): only the rows of
+# the accepted frontier are read.
+PATH_WALK = {"tree-path"}
 DEFAULT_WORKLOAD = "smollm2"
 
 
@@ -264,7 +268,7 @@ def step_bytes(cfg) -> int:
 class Runner:
     """Pre-marshalled C-ABI calls, one per rotating input set."""
 
-    def __init__(self, sv, cfg, inputs, nsets, dev):
+    def __init__(self, sv, cfg, inputs, nsets, dev, path_walk=False):
         import torch
         from draft_token_verification_sv_gb300 import _native as N
         from draft_token_verification_sv_gb300.verify import chain_desc
@@ -282,7 +286,8 @@ class Runner:
             d.dtype = N.SV_BF16 if cfg.dtype == "bf16" else N.SV_F32
             d.row_stride = cfg.vocab
             self.desc = d
-            ws_need = self.lib.sv_tree_workspace_size(ctypes.byref(d))
+            ws_need = (self.lib.sv_tree_path_workspace_size if path_walk else
+                       self.lib.sv_tree_workspace_size)(ctypes.byref(d))
         else:
             d = chain_desc(inputs["target"], inputs["draft"], cfg.temperature, cfg.top_p, inputs["d2t"])
             self.desc = d
@@ -313,7 +318,8 @@ class Runner:
                         vp(o["tokens"]), vp(o["k"]), None, None, vp(o["status"]), vp(self.ws),
                         ctypes.c_size_t(self.ws.numel()))
             self.sets.append(args)
-        self.fn = self.lib.sv_verify_tree if self.tree else self.lib.sv_verify_chain
+        self.fn = (self.lib.sv_verify_tree_path if path_walk else self.lib.sv_verify_tree) if self.tree \
+            else self.lib.sv_verify_chain
 
     def step(self, s: int, stream_handle):
         st = self.fn(*self.sets[s % len(self.sets)], stream_handle)
@@ -340,7 +346,10 @@ def run_ours(args, dist: Dist):
     cfg = WORKLOADS[args.workload]
     inputs = make_inputs(cfg, dev, sv)
     nsets = n_sets_for(cfg)
-    R = Runner(sv, cfg, inputs, nsets, dev)
+    if args.workload in PATH_WALK:
+        nsets = max(nsets, 4)  # the walk reads a fifth of the rows: rotate further
+    walk = args.workload in PATH_WALK
+    R = Runner(sv, cfg, inputs, nsets, dev, path_walk=walk)
     lib = R.lib
     stream = torch.cuda.Stream(device=dev)
     sh = ctypes.c_void_p(stream.cuda_stream)
@@ -416,7 +425,7 @@ def run_ours(args, dist: Dist):
     value = tot_units / (t_max / 1e3)
 
     # End to end through the public call, pinned host inputs each step.
-    e2e = run_e2e(cfg, inputs, sv, dev, stream, K, dist)
+    e2e = run_e2e(cfg, inputs, sv, dev, stream, K, dist, path_walk=walk)
 
     peak, peak_kind = hbm_peak()
     dom = 0
@@ -424,7 +433,15 @@ def run_ours(args, dist: Dist):
     if not R.tree:
         dom_name = "greedy_kernel(chain)" if cfg.temperature == 0 else (
             "topp_slice_kernel" if cfg.top_p < 1 else "stats_stream_kernel")
-    achieved = step_bytes(cfg) / (avg_phase[dom] / 1e3) / 1e9
+    bytes_dom, ms_dom = step_bytes(cfg), avg_phase[dom]
+    if walk:
+        # Rows read: (accept_len + 1) per tree (distinct sibling tokens), over
+        # every level launch (phase 0 is the validation launch).
+        acc = R.out["k"].cpu().numpy().astype(np.int64)
+        bytes_dom = int((acc + 1).sum()) * cfg.vocab * (2 if cfg.dtype == "bf16" else 4)
+        ms_dom = sum(avg_phase[1:])
+        dom_name = "walk_level_kernel (all levels)"
+    achieved = bytes_dom / (ms_dom / 1e3) / 1e9
     traffic = ncu_traffic(args.workload, dom_name)
     res = {
         "metric": "verify rows/s (B*(2*gamma+1) rows per chain step, B*N per tree step)",
@@ -440,11 +457,11 @@ def run_ours(args, dist: Dist):
         "dtype": "bf16" if cfg.dtype == "bf16" else "f32",
         "data": "synthetic (seeded, shapes and value recipe of the pages' settings)",
         "config": config_of(cfg, args.workload, nsets, dist.world),
-        "hbm_gbs_algorithmic": step_bytes(cfg) * K / (elapsed / 1e3) / 1e9,
+        "hbm_gbs_algorithmic": (bytes_dom if walk else step_bytes(cfg)) * K / (elapsed / 1e3) / 1e9,
         "roofline": {"bound": "hbm", "kernel": dom_name, "achieved": achieved, "peak": peak,
                      "peak_source": f"hbm_gbs of {peak_kind}", "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": traffic, "bytes_per_launch": step_bytes(cfg),
-                     "avg_launch_ms": avg_phase[dom]},
+                     "traffic": traffic, "bytes_per_launch": bytes_dom,
+                     "avg_launch_ms": ms_dom},
         "phase_ms": avg_phase,
         "gpu_launches": launches,
         "e2e": e2e,
@@ -469,7 +486,7 @@ def config_of(cfg, workload, nsets, world):
     return c
 
 
-def run_e2e(cfg, inputs, sv, dev, stream, K, dist):
+def run_e2e(cfg, inputs, sv, dev, stream, K, dist, path_walk=False):
     import torch
     tree = isinstance(cfg, synth.TreeConfig)
     names = ["logits", "parents", "tokens"] if tree else \
@@ -488,7 +505,7 @@ def run_e2e(cfg, inputs, sv, dev, stream, K, dist):
         for n in names:
             devb[n].copy_(host[n], non_blocking=True)
         if tree:
-            o = sv.verify_tree(devb["logits"], devb["parents"], devb["tokens"], cfg.max_depth)
+            o = sv.verify_tree(devb["logits"], devb["parents"], devb["tokens"], cfg.max_depth, path_walk=path_walk)
             out_host.copy_(o["out_tokens"], non_blocking=True)
             k_host.copy_(o["accept_len"], non_blocking=True)
         else:

@@ -67,6 +67,8 @@ SIGNATURES = {
     "sv_static_scratch_bytes": (_SZ, []),
     "sv_tree_workspace_size": (_SZ, [ctypes.POINTER(TreeDesc)]),
     "sv_verify_tree": (_I32, [ctypes.POINTER(TreeDesc), _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "sv_tree_path_workspace_size": (_SZ, [ctypes.POINTER(TreeDesc)]),
+    "sv_verify_tree_path": (_I32, [ctypes.POINTER(TreeDesc), _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "sv_d2t_scatter": (_I32, [_P, _I64, _P, _P, _I32, _I32, _I32, _I32, _F, _P, _I64, _P]),
     "sv_build_t2d": (_I32, [_P, _I32, _I32, _P, _P, _P]),
     "sv_sample_workspace_size": (_SZ, [ctypes.POINTER(SampleDesc)]),

@@ -159,6 +159,26 @@ sv_status sv_verify_tree(const sv_tree_desc* desc, const void* logits, const int
                      workspace, reinterpret_cast<cudaStream_t>(stream));
 }
 
+size_t sv_tree_path_workspace_size(const sv_tree_desc* desc) {
+  if (!tree_desc_ok(desc)) return 0;
+  return tree_walk_workspace_bytes(*desc);
+}
+
+sv_status sv_verify_tree_path(const sv_tree_desc* desc, const void* logits, const int32_t* parents,
+                              const int32_t* tokens, int32_t* accept_len, int32_t* path,
+                              int32_t* out_tokens, int32_t* row_status, void* workspace,
+                              size_t workspace_bytes, sv_stream_t stream) {
+  CallScope scope;
+  if (!tree_desc_ok(desc)) return SV_ERR_INVALID_ARGUMENT;
+  if (desc->batch == 0) return SV_OK;
+  if (!logits || !aligned_elem(logits, desc->dtype) || !parents || !tokens || !accept_len || !path ||
+      !out_tokens || !workspace)
+    return SV_ERR_INVALID_ARGUMENT;
+  if (workspace_bytes < sv_tree_path_workspace_size(desc)) return SV_ERR_WORKSPACE_TOO_SMALL;
+  return greedy_tree_walk(*desc, logits, parents, tokens, accept_len, path, out_tokens, row_status,
+                          workspace, reinterpret_cast<cudaStream_t>(stream));
+}
+
 sv_status sv_d2t_scatter(const void* draft_logits, int64_t in_row_stride, const int32_t* d2t,
                          const int32_t* t2d, int32_t rows, int32_t draft_vocab, int32_t vocab,
                          sv_dtype dtype, float fill, void* out, int64_t out_row_stride,

@@ -92,6 +92,12 @@ sv_status greedy_tree(const sv_tree_desc& d, const void* logits, const int32_t* 
                       cudaStream_t stream);
 sv_status greedy_sample(const sv_sample_desc& d, const void* logits, int32_t* out_tokens,
                         float* out_prob, cudaStream_t stream);
+// Tree verify along the accepted frontier only (sv_tree_walk.cu).
+size_t tree_walk_workspace_bytes(const sv_tree_desc& d);
+sv_status greedy_tree_walk(const sv_tree_desc& d, const void* logits, const int32_t* parents,
+                           const int32_t* tokens, int32_t* accept_len, int32_t* path,
+                           int32_t* out_tokens, int32_t* row_status, void* workspace,
+                           cudaStream_t stream);
 
 struct ChainArgs {
   sv_chain_desc d;

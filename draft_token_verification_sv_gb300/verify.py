@@ -143,8 +143,10 @@ def verify_chain(target: torch.Tensor, draft: torch.Tensor | None, draft_ids: to
 
 
 def verify_tree(logits: torch.Tensor, parents: torch.Tensor, tokens: torch.Tensor, max_depth: int,
-                *, out: dict | None = None, ws: torch.Tensor | None = None, stream=None) -> dict:
-    """Greedy verify of B draft trees; see sv_verify_tree.
+                *, out: dict | None = None, ws: torch.Tensor | None = None, stream=None,
+                path_walk: bool = False) -> dict:
+    """Greedy verify of B draft trees; see sv_verify_tree (path_walk:
+    sv_verify_tree_path, which reads only the rows of the accepted frontier).
 
     logits [B, N, V], parents/tokens [B, N] int32.  Returns dict(accept_len
     [B], path [B, D+1], out_tokens [B, D+1], row_status [B]).
@@ -163,14 +165,16 @@ def verify_tree(logits: torch.Tensor, parents: torch.Tensor, tokens: torch.Tenso
                    path=torch.empty((B, L), dtype=torch.int32, device=dev),
                    out_tokens=torch.empty((B, L), dtype=torch.int32, device=dev),
                    row_status=torch.empty(B, dtype=torch.int32, device=dev))
-    need = N.lib().sv_tree_workspace_size(ctypes.byref(d))
+    lib = N.lib()
+    size_fn, fn, name = ((lib.sv_tree_path_workspace_size, lib.sv_verify_tree_path, "sv_verify_tree_path")
+                         if path_walk else (lib.sv_tree_workspace_size, lib.sv_verify_tree, "sv_verify_tree"))
+    need = size_fn(ctypes.byref(d))
     if ws is None:
         ws = workspace(need, dev, stream)
-    st = N.lib().sv_verify_tree(ctypes.byref(d), _p(logits), _p(_i32(parents, "parents")),
-                                _p(_i32(tokens, "tokens")), _p(out["accept_len"]), _p(out["path"]),
-                                _p(out["out_tokens"]), _p(out.get("row_status")), _p(ws),
-                                ctypes.c_size_t(ws.numel()), _stream(stream))
-    N.check(st, "sv_verify_tree")
+    st = fn(ctypes.byref(d), _p(logits), _p(_i32(parents, "parents")), _p(_i32(tokens, "tokens")),
+            _p(out["accept_len"]), _p(out["path"]), _p(out["out_tokens"]), _p(out.get("row_status")), _p(ws),
+            ctypes.c_size_t(ws.numel()), _stream(stream))
+    N.check(st, name)
     return out
 
 

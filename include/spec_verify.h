@@ -213,6 +213,25 @@ sv_status sv_verify_tree(const sv_tree_desc* desc, const void* logits,
                          sv_stream_t stream);
 
 /*
+ * The same greedy tree verify, reading only the rows of the accepted
+ * frontier ([P2] §5 tree; the accepted nodes of depth d are the only rows
+ * that decide depth d+1).  One launch per level, depth 0..D: level d takes
+ * the argmax of the rows of the accepted depth-d nodes and keeps their
+ * children whose token matches; the walk ends at the first empty level.  It
+ * reads (accept_len + 1) rows per tree when sibling tokens are distinct,
+ * instead of N.  Arguments, layouts and results are those of
+ * sv_verify_tree, with one difference: SV_ROW_EMPTY is reported only for a
+ * row the walk reads (rows off the walked path are never read).
+ * Workspace: sv_tree_path_workspace_size (scratch, no initialisation).
+ */
+size_t sv_tree_path_workspace_size(const sv_tree_desc* desc);
+sv_status sv_verify_tree_path(const sv_tree_desc* desc, const void* logits,
+                              const int32_t* parents, const int32_t* tokens,
+                              int32_t* accept_len, int32_t* path, int32_t* out_tokens,
+                              int32_t* row_status, void* workspace, size_t workspace_bytes,
+                              sv_stream_t stream);
+
+/*
  * EAGLE3 scatter of small-vocabulary draft logits into the target
  * vocabulary ([P1] §六 compute_logits): out[r, d2t[j]] = in[r, j] for
  * j < draft_vocab; every other entry of the row is `fill` (normally -INFINITY).
