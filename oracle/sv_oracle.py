@@ -468,3 +468,16 @@ def verify_tree(logits, parents, tokens, max_depth, rows=None) -> dict:
         out["out_tokens"][b] = r["out_tokens"]
         out["status"][b] = r["status"]
     return out
+
+
+# ---------------------------------------------------------------------------
+# Top-k node expansion of a draft tree ([P2] §5: every node expanded into its
+# top_k draft tokens)
+# ---------------------------------------------------------------------------
+
+def top_k(logits: np.ndarray, k: int) -> np.ndarray:
+    """The ids of the k highest logits of a row, in descending logit order,
+    equal logits by lower id (the same ranking as the top-p filter).  -inf
+    logits rank last, by id.  Requires 1 <= k <= len(row)."""
+    logits = np.asarray(logits, dtype=np.float64)
+    return nucleus_order(logits)[:k].astype(np.int64)

@@ -8,6 +8,7 @@
   greedy decoding)
 - greedy tree == autoregressive greedy, deepest consistent node
 - compact draft row + d2t == scattered draft row (EAGLE3 section of the SSD page)
+- top-k node expansion == repeated selection of the largest remaining logit
 """
 import itertools
 import math
@@ -278,3 +279,43 @@ def test_bf16_generator_rounding_matches_torch():
     x[:4] = [0.0, -0.0, 1.0, -1.0]
     want = torch.from_numpy(x).to(torch.bfloat16).float().numpy()
     np.testing.assert_array_equal(bf16_bits_to_f32(to_bf16_bits(x)), want)
+
+
+# --- top-k node expansion ("A 2.16x speculative-decoding speedup ..." §5) ---
+
+def _top_k_rows():
+    rows = []
+    for ln in open(os.path.join(GOLDEN, "top_k_rows.txt")):
+        if ln.startswith("#") or not ln.strip():
+            continue
+        k, lg, ids = [c.strip() for c in ln.split("|")]
+        rows.append((int(k), np.array([float(x) for x in lg.split()]), [int(x) for x in ids.split()]))
+    return rows
+
+
+@pytest.mark.parametrize("row", _top_k_rows())
+def test_golden_top_k_rows(row):
+    k, logits, ids = row
+    assert O.top_k(logits, k).tolist() == ids
+
+
+@pytest.mark.parametrize("seed", range(20))
+def test_top_k_equals_repeated_selection(seed):
+    """Brute force: take the largest remaining logit k times (lowest id among
+    equal ones) -- no sort involved."""
+    g = np.random.default_rng(seed)
+    V = int(g.integers(1, 60))
+    x = np.round(g.normal(0, 2, V))            # many ties
+    if seed % 4 == 0:
+        x[g.integers(0, V, size=max(1, V // 3))] = -np.inf
+    k = int(g.integers(1, V + 1))
+    left = list(range(V))
+    want = []
+    for _ in range(k):
+        best = left[0]
+        for j in left[1:]:
+            if x[j] > x[best]:
+                best = j
+        want.append(best)
+        left.remove(best)
+    assert O.top_k(x, k).tolist() == want
