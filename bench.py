@@ -49,7 +49,10 @@ WORKLOADS = {
     "qwen3-d2t": synth.QWEN3_D2T,
     "tree": synth.TREE,
     "tree-path": synth.TREE,
+    "tree-topk": synth.TREE,
 }
+# Top-k node expansion (sv_topk, k = 8) over the tree workload's node rows.
+TOPK = {"tree-topk": 8}
 # Workloads verified by the path walk (sv_verify_tree_path): only the rows of
 # the accepted frontier are read.
 PATH_WALK = {"tree-path"}
@@ -268,7 +271,7 @@ def step_bytes(cfg) -> int:
 class Runner:
     """Pre-marshalled C-ABI calls, one per rotating input set."""
 
-    def __init__(self, sv, cfg, inputs, nsets, dev, path_walk=False):
+    def __init__(self, sv, cfg, inputs, nsets, dev, path_walk=False, topk=0):
         import torch
         from draft_token_verification_sv_gb300 import _native as N
         from draft_token_verification_sv_gb300.verify import chain_desc
@@ -320,6 +323,15 @@ class Runner:
             self.sets.append(args)
         self.fn = (self.lib.sv_verify_tree_path if path_walk else self.lib.sv_verify_tree) if self.tree \
             else self.lib.sv_verify_chain
+        if topk:
+            # Every node row of every tree: R = B*N rows, k ids each.
+            kd = N.TopkDesc()
+            kd.rows, kd.vocab, kd.k = cfg.batch * cfg.nodes, cfg.vocab, topk
+            kd.dtype, kd.row_stride = self.desc.dtype, cfg.vocab
+            self.kdesc = kd
+            self.out["ids"] = torch.empty((cfg.batch * cfg.nodes, topk), dtype=torch.int32, device=dev)
+            self.sets = [(ctypes.byref(kd), a[1], vp(self.out["ids"]), None) for a in self.sets]
+            self.fn = self.lib.sv_topk
 
     def step(self, s: int, stream_handle):
         st = self.fn(*self.sets[s % len(self.sets)], stream_handle)
@@ -349,7 +361,7 @@ def run_ours(args, dist: Dist):
     if args.workload in PATH_WALK:
         nsets = max(nsets, 4)  # the walk reads a fifth of the rows: rotate further
     walk = args.workload in PATH_WALK
-    R = Runner(sv, cfg, inputs, nsets, dev, path_walk=walk)
+    R = Runner(sv, cfg, inputs, nsets, dev, path_walk=walk, topk=TOPK.get(args.workload, 0))
     lib = R.lib
     stream = torch.cuda.Stream(device=dev)
     sh = ctypes.c_void_p(stream.cuda_stream)
@@ -425,11 +437,13 @@ def run_ours(args, dist: Dist):
     value = tot_units / (t_max / 1e3)
 
     # End to end through the public call, pinned host inputs each step.
-    e2e = run_e2e(cfg, inputs, sv, dev, stream, K, dist, path_walk=walk)
+    e2e = run_e2e(cfg, inputs, sv, dev, stream, K, dist, path_walk=walk, topk=TOPK.get(args.workload, 0))
 
     peak, peak_kind = hbm_peak()
     dom = 0
     dom_name = {True: "greedy_kernel(tree)", False: None}[R.tree]
+    if args.workload in TOPK:
+        dom_name = "topk_kernel"
     if not R.tree:
         dom_name = "greedy_kernel(chain)" if cfg.temperature == 0 else (
             "topp_slice_kernel" if cfg.top_p < 1 else "stats_stream_kernel")
@@ -486,25 +500,32 @@ def config_of(cfg, workload, nsets, world):
     return c
 
 
-def run_e2e(cfg, inputs, sv, dev, stream, K, dist, path_walk=False):
+def run_e2e(cfg, inputs, sv, dev, stream, K, dist, path_walk=False, topk=0):
     import torch
     tree = isinstance(cfg, synth.TreeConfig)
     names = ["logits", "parents", "tokens"] if tree else \
         ["target", "draft", "ids", "u_accept", "u_resample"]
+    if topk:
+        names = ["logits"]
     if not tree and cfg.temperature == 0:
         names = ["target", "ids"]
     host = {n: inputs[n].cpu().pin_memory() for n in names}
     devb = {n: torch.empty_like(inputs[n]) for n in names}
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     L = cfg.max_depth + 1 if tree else cfg.gamma + 1
+    if topk:
+        L = cfg.nodes * topk
     out_host = torch.empty((cfg.batch, L), dtype=torch.int32).pin_memory()
     k_host = torch.empty(cfg.batch, dtype=torch.int32).pin_memory()
-    d2h = out_host.numel() * 4 + k_host.numel() * 4
+    d2h = out_host.numel() * 4 + (0 if topk else k_host.numel() * 4)
 
     def one():
         for n in names:
             devb[n].copy_(host[n], non_blocking=True)
-        if tree:
+        if topk:
+            ids = sv.topk(devb["logits"].reshape(cfg.batch * cfg.nodes, cfg.vocab), topk)
+            out_host.copy_(ids.reshape(cfg.batch, -1), non_blocking=True)
+        elif tree:
             o = sv.verify_tree(devb["logits"], devb["parents"], devb["tokens"], cfg.max_depth, path_walk=path_walk)
             out_host.copy_(o["out_tokens"], non_blocking=True)
             k_host.copy_(o["accept_len"], non_blocking=True)

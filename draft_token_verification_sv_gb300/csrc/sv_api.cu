@@ -179,6 +179,17 @@ sv_status sv_verify_tree_path(const sv_tree_desc* desc, const void* logits, cons
                           workspace, reinterpret_cast<cudaStream_t>(stream));
 }
 
+sv_status sv_topk(const sv_topk_desc* desc, const void* logits, int32_t* out_ids, float* out_vals,
+                  sv_stream_t stream) {
+  CallScope scope;
+  if (!desc || desc->rows < 0 || !valid_vocab(desc->vocab) || !valid_dtype(desc->dtype)) return SV_ERR_INVALID_ARGUMENT;
+  if (desc->k < 1 || desc->k > SV_MAX_TOPK || desc->k > desc->vocab) return SV_ERR_INVALID_ARGUMENT;
+  if (!valid_stride(desc->row_stride, desc->vocab, desc->dtype)) return SV_ERR_INVALID_ARGUMENT;
+  if (desc->rows == 0) return SV_OK;
+  if (!logits || !aligned_elem(logits, desc->dtype) || !out_ids) return SV_ERR_INVALID_ARGUMENT;
+  return topk_rows(*desc, logits, out_ids, out_vals, reinterpret_cast<cudaStream_t>(stream));
+}
+
 sv_status sv_d2t_scatter(const void* draft_logits, int64_t in_row_stride, const int32_t* d2t,
                          const int32_t* t2d, int32_t rows, int32_t draft_vocab, int32_t vocab,
                          sv_dtype dtype, float fill, void* out, int64_t out_row_stride,

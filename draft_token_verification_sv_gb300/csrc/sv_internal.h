@@ -92,6 +92,9 @@ sv_status greedy_tree(const sv_tree_desc& d, const void* logits, const int32_t* 
                       cudaStream_t stream);
 sv_status greedy_sample(const sv_sample_desc& d, const void* logits, int32_t* out_tokens,
                         float* out_prob, cudaStream_t stream);
+// Top-k ids per row (sv_topk.cu).
+sv_status topk_rows(const sv_topk_desc& d, const void* logits, int32_t* out_ids, float* out_vals,
+                    cudaStream_t stream);
 // Tree verify along the accepted frontier only (sv_tree_walk.cu).
 size_t tree_walk_workspace_bytes(const sv_tree_desc& d);
 sv_status greedy_tree_walk(const sv_tree_desc& d, const void* logits, const int32_t* parents,

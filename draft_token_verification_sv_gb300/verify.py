@@ -178,6 +178,24 @@ def verify_tree(logits: torch.Tensor, parents: torch.Tensor, tokens: torch.Tenso
     return out
 
 
+def topk(logits: torch.Tensor, k: int, *, values: bool = False, stream=None):
+    """Top-k node expansion; see sv_topk.  logits [R, V] -> ids [R, k] int32
+    (and their logits [R, k] float32 when ``values``)."""
+    _cuda(logits, "logits")
+    if logits.dim() != 2:
+        raise ValueError("logits must be [rows, vocab]")
+    R, V = logits.shape
+    d = N.TopkDesc()
+    d.rows, d.vocab, d.k = R, V, int(k)
+    d.dtype = _code(logits)
+    d.row_stride = _row_stride(logits, "logits")
+    ids = torch.empty((R, int(k)), dtype=torch.int32, device=logits.device)
+    vals = torch.empty((R, int(k)), dtype=torch.float32, device=logits.device) if values else None
+    st = N.lib().sv_topk(ctypes.byref(d), _p(logits), _p(ids), _p(vals), _stream(stream))
+    N.check(st, "sv_topk")
+    return (ids, vals) if values else ids
+
+
 def d2t_scatter(draft_logits: torch.Tensor, d2t: torch.Tensor, vocab: int, fill: float = -math.inf,
                 t2d: torch.Tensor | None = None, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """Scatter [R, V_d] draft logits into [R, vocab]; see sv_d2t_scatter."""

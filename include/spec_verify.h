@@ -70,6 +70,7 @@ typedef enum sv_dtype { SV_F32 = 0, SV_BF16 = 1 } sv_dtype;
 /* Limits checked on the host. */
 #define SV_MAX_GAMMA 64
 #define SV_MAX_VOCAB 16777216
+#define SV_MAX_TOPK 16
 #define SV_MAX_TREE_NODES 1024
 #define SV_MAX_TREE_DEPTH 64
 
@@ -230,6 +231,28 @@ sv_status sv_verify_tree_path(const sv_tree_desc* desc, const void* logits,
                               int32_t* accept_len, int32_t* path, int32_t* out_tokens,
                               int32_t* row_status, void* workspace, size_t workspace_bytes,
                               sv_stream_t stream);
+
+/*
+ * Top-k node expansion for building a draft token tree ([P2] §5: every node
+ * grows into its top_k draft tokens): the k ids with the highest logits of
+ * each row, in descending logit order, equal logits by lower id (-inf ranks
+ * last, by id).  NaN logits are never chosen: a row with fewer than k logits
+ * that are not NaN ends in ids -1 and values NaN.  No workspace.
+ *
+ *   logits   [rows] rows of vocab elements (dtype), stride row_stride (>= vocab).
+ *   out_ids  [rows, k] int32.
+ *   out_vals optional [rows, k] float: the logits of those ids.
+ */
+typedef struct sv_topk_desc {
+  int32_t rows;        /* R >= 0 */
+  int32_t vocab;       /* V in [1, SV_MAX_VOCAB] */
+  int32_t k;           /* k in [1, min(V, SV_MAX_TOPK)] */
+  sv_dtype dtype;
+  int64_t row_stride;
+} sv_topk_desc;
+
+sv_status sv_topk(const sv_topk_desc* desc, const void* logits, int32_t* out_ids, float* out_vals,
+                  sv_stream_t stream);
 
 /*
  * EAGLE3 scatter of small-vocabulary draft logits into the target

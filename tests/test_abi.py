@@ -222,3 +222,36 @@ def test_missing_library_fails_loudly(N, tmp_path, monkeypatch):
     monkeypatch.setattr(N, "_lib", None)
     with pytest.raises(RuntimeError, match="missing"):
         N.lib()
+
+
+def _topk(N, **kw):
+    d = N.TopkDesc()
+    d.rows, d.vocab, d.k, d.dtype, d.row_stride = 4, 1000, 8, N.SV_BF16, 1000
+    for k, v in kw.items():
+        setattr(d, k, v)
+    return d
+
+
+@pytest.mark.parametrize("field,value", [("k", 0), ("k", 17), ("vocab", 0), ("rows", -1), ("row_stride", 999)])
+def test_topk_rejects_bad_descriptor(N, field, value):
+    d = _topk(N, **{field: value})
+    assert N.lib().sv_topk(ctypes.byref(d), A, A, None, None) == N.SV_ERR_INVALID_ARGUMENT
+
+
+def test_topk_k_above_vocab_and_pointers(N):
+    f = N.lib().sv_topk
+    E = N.SV_ERR_INVALID_ARGUMENT
+    assert f(ctypes.byref(_topk(N, vocab=5, row_stride=5, k=6)), A, A, None, None) == E
+    assert f(ctypes.byref(_topk(N)), None, A, None, None) == E
+    assert f(ctypes.byref(_topk(N)), MIS, A, None, None) == E
+    assert f(ctypes.byref(_topk(N)), A, None, None, None) == E
+
+
+def test_tree_path_pointer_and_workspace_checks(N):
+    d = _tree(N)
+    need = N.lib().sv_tree_path_workspace_size(ctypes.byref(d))
+    assert need >= 2 * 32 * (4 + 8)
+    f = N.lib().sv_verify_tree_path
+    assert f(ctypes.byref(d), None, A, A, A, A, A, None, A, ctypes.c_size_t(need), None) == 1
+    assert f(ctypes.byref(d), A, A, A, A, A, A, None, A, ctypes.c_size_t(need - 1), None) == 4
+    assert f(ctypes.byref(_tree(N, nodes=0)), A, A, A, A, A, A, None, A, ctypes.c_size_t(need), None) == 1
