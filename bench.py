@@ -158,6 +158,8 @@ KERNEL_SOURCES = {
     "decide_kernel": "sv_decide.cu",
     "greedy_kernel(chain)": "sv_greedy.cu",
     "greedy_kernel(tree)": "sv_greedy.cu",
+    "topk_kernel": "sv_topk.cu",
+    "walk_level_kernel (all levels)": "sv_tree_walk.cu",
 }
 
 
