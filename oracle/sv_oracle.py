@@ -31,10 +31,12 @@ Status bits follow the library's public convention so tests can compare them;
 they are restated here, not imported.
 
 Parity pins (tests/test_oracle_*.py): the speculative-sampling theorem by
-exact enumeration, q == p acceptance, greedy == autoregressive greedy on a
-prefix-conditioned toy model, an O(V^2) per-element statement of top-p,
-closed-form golden rows, compact-vs-scattered d2t, and brute-force tree
-paths.  No function here is "parity unpinned".
+exact enumeration (for the chain and for the sampled tree), q == p
+acceptance, greedy == autoregressive greedy on a prefix-conditioned toy
+model, an O(V^2) per-element statement of top-p, closed-form golden rows,
+compact-vs-scattered d2t, brute-force tree paths, a one-child-per-node tree
+against the chain, and repeated-argmax top-k.  No function here is "parity
+unpinned".
 """
 from __future__ import annotations
 
@@ -467,6 +469,149 @@ def verify_tree(logits, parents, tokens, max_depth, rows=None) -> dict:
         out["path"][b] = r["path"]
         out["out_tokens"][b] = r["out_tokens"]
         out["status"][b] = r["status"]
+    return out
+
+
+# ---------------------------------------------------------------------------
+# Token-tree speculative sampling verify (T > 0) over the [P2] §5 tree shape
+# ---------------------------------------------------------------------------
+
+def _tree_checks(parents: np.ndarray, tokens: np.ndarray, vocab: int, max_depth: int):
+    """Status bits of a tree's shape and tokens, and node depths."""
+    N = parents.shape[0]
+    status = 0
+    if parents[0] != -1:
+        status |= STATUS_BAD_PARENT
+    for n in range(1, N):
+        if not (0 <= parents[n] < n):
+            status |= STATUS_BAD_PARENT
+        if not (0 <= tokens[n] < vocab):
+            status |= STATUS_BAD_TOKEN
+    depth = np.zeros(N, np.int64)
+    if not status & STATUS_BAD_PARENT:
+        for n in range(1, N):
+            depth[n] = depth[parents[n]] + 1
+        if depth.max() > max_depth:
+            status |= STATUS_DEPTH_EXCEEDED
+    return status, depth
+
+
+def verify_tree_sample_row(target_logits: np.ndarray, draft_logits: np.ndarray,
+                           parents: np.ndarray, tokens: np.ndarray,
+                           u_accept: np.ndarray, u_final: float,
+                           temperature: float, top_p: float, max_depth: int,
+                           trace: list | None = None) -> dict:
+    """Speculative-sampling verify of one draft token tree.
+
+    target_logits [N, V]: the target's logits at every node (row n predicts
+    the token after n's root path, as in the greedy tree).  draft_logits
+    [N, V]: the draft's logits at every node; n's children are the draft's
+    samples from dist(draft row n).  parents/tokens as for the greedy tree.
+    u_accept [N]: the uniform of each node's accept test (entry 0 unused).
+    u_final: one uniform for the token drawn after the accepted path.
+
+    READING (the pages give the tree's shape, [P2] §5, and the rule for one
+    draft per position, [P3] §3.1, but no rule for several drafts at one
+    position): sequential per-child rejection with a residual update.  At an
+    accepted node with p = dist(target row), q = dist(draft row) (same T and
+    top_p, [P3] §6.2) the residual starts as r = p.  The children are tested
+    in increasing node order: a child with token x is accepted iff
+    u * q(x) < r(x) (the chain's rule with p replaced by r); a rejection
+    replaces r by norm(max(0, r - q)) (if that has no mass -- impossible in
+    exact arithmetic for a child the draft could have drawn -- r is kept and
+    the fallback bit is set).  The first accepted child becomes the current
+    node.  When every child is rejected the last token is drawn from r; at a
+    node without children it is the bonus token drawn from p.  Every test is
+    one-draft speculative sampling against the current residual, so the
+    emitted tokens follow the target whenever each node's children are
+    independent draws from that node's q.
+
+    ``trace`` (optional list) receives one dict per accept test (node,
+    token, threshold = min(1, r(x)/q(x)) -- 1 when q(x) = 0 < r(x) --,
+    accepted) and a final dict(final=True, weights) with the distribution
+    the last token was drawn from.
+
+    Returns dict(accept_len, path [max_depth+1], out_tokens [max_depth+1]
+    (-1 padded), status, margin, resample_fallback).
+    """
+    target_logits = np.asarray(target_logits, dtype=np.float64)
+    draft_logits = np.asarray(draft_logits, dtype=np.float64)
+    parents = np.asarray(parents, dtype=np.int64)
+    tokens = np.asarray(tokens, dtype=np.int64)
+    N, V = target_logits.shape
+    L = max_depth + 1
+    res = dict(accept_len=0, path=np.full(L, -1, np.int64), out_tokens=np.full(L, -1, np.int64),
+               status=0, margin=np.inf, resample_fallback=False)
+    status, _ = _tree_checks(parents, tokens, V, max_depth)
+    if not (np.all(np.any(np.isfinite(target_logits), axis=1))
+            and np.all(np.any(np.isfinite(draft_logits), axis=1))):
+        status |= STATUS_EMPTY_ROW
+    if status:
+        res["status"] = status
+        return res
+    margins = []
+    node, chain = 0, [0]
+    while True:
+        p, mg_p = dist(target_logits[node], temperature, top_p)
+        q, mg_q = dist(draft_logits[node], temperature, top_p)
+        margins += [mg_p, mg_q]
+        r = p.copy()
+        nxt = None
+        for c in range(node + 1, N):
+            if parents[c] != node:
+                continue
+            x = tokens[c]
+            u = float(u_accept[c])
+            accept = u * q[x] < r[x]
+            if q[x] > 0.0:
+                threshold = min(1.0, r[x] / q[x])
+                margins.append(abs(u - r[x] / q[x]))
+            else:
+                threshold = 1.0 if r[x] > 0.0 else 0.0
+            if trace is not None:
+                trace.append(dict(node=c, token=int(x), threshold=threshold, accepted=bool(accept)))
+            if accept:
+                nxt = c
+                break
+            residual = np.maximum(0.0, r - q)
+            if residual.sum() > 0.0:
+                r = residual / residual.sum()
+            else:
+                res["resample_fallback"] = True
+        if nxt is None:
+            break
+        node = nxt
+        chain.append(node)
+    # r is p when the node has no children, else the residual after the last rejection.
+    tok, mg = inverse_cdf(r, float(u_final))
+    margins.append(mg)
+    if trace is not None:
+        trace.append(dict(final=True, weights=r / r.sum()))
+    d = len(chain) - 1
+    res["accept_len"] = d
+    res["path"][: d + 1] = chain
+    res["out_tokens"][:d] = tokens[chain[1:]]
+    res["out_tokens"][d] = tok
+    res["margin"] = float(min(margins))
+    return res
+
+
+def verify_tree_sample(target_logits, draft_logits, parents, tokens, u_accept, u_final,
+                       temperature, top_p, max_depth, rows=None) -> dict:
+    """Batched tree sampling verify: logits [B, N, V], parents/tokens/u_accept
+    [B, N], u_final [B]."""
+    target_logits = np.asarray(target_logits)
+    B = target_logits.shape[0]
+    L = max_depth + 1
+    out = dict(accept_len=np.zeros(B, np.int64), path=np.full((B, L), -1, np.int64),
+               out_tokens=np.full((B, L), -1, np.int64), status=np.zeros(B, np.int64),
+               margin=np.full(B, np.inf), resample_fallback=np.zeros(B, bool))
+    for b in (range(B) if rows is None else rows):
+        r = verify_tree_sample_row(target_logits[b], np.asarray(draft_logits)[b], np.asarray(parents)[b],
+                                   np.asarray(tokens)[b], np.asarray(u_accept)[b],
+                                   float(np.asarray(u_final)[b]), temperature, top_p, max_depth)
+        for k in ("accept_len", "path", "out_tokens", "status", "margin", "resample_fallback"):
+            out[k][b] = r[k]
     return out
 
 
