@@ -50,6 +50,7 @@ WORKLOADS = {
     "tree": synth.TREE,
     "tree-path": synth.TREE,
     "tree-topk": synth.TREE,
+    "tree-sample": synth.TREE_SAMPLE,
 }
 # Top-k node expansion (sv_topk, k = 8) over the tree workload's node rows.
 TOPK = {"tree-topk": 8}
@@ -159,6 +160,7 @@ KERNEL_SOURCES = {
     "greedy_kernel(chain)": "sv_greedy.cu",
     "greedy_kernel(tree)": "sv_greedy.cu",
     "topk_kernel": "sv_topk.cu",
+    "tree_sample_kernel": "sv_tree_sample.cu",
     "walk_level_kernel (all levels)": "sv_tree_walk.cu",
 }
 
@@ -234,6 +236,16 @@ def make_inputs(cfg, dev, sv):
     """Seeded inputs on the device, plus draft ids drawn by the library's
     draft sampler from the uniforms (outside any timed region)."""
     import torch
+    if isinstance(cfg, synth.TreeSampleConfig):
+        x = synth.make_tree_sample_inputs(cfg)
+
+        def as_t(store):
+            t = torch.from_numpy(np.ascontiguousarray(store).view(np.int16)).view(torch.bfloat16) \
+                if cfg.dtype == "bf16" else torch.from_numpy(store)
+            return t.to(dev)
+        return dict(host=x, logits=as_t(x["logits_store"]), draft=as_t(x["draft_store"]),
+                    parents=torch.from_numpy(x["parents"]).to(dev), tokens=torch.from_numpy(x["tokens"]).to(dev),
+                    u_accept=torch.from_numpy(x["u_accept"]).to(dev), u_final=torch.from_numpy(x["u_final"]).to(dev))
     if isinstance(cfg, synth.TreeConfig):
         x = synth.make_tree_inputs(cfg)
         store = x["logits_store"]
@@ -281,10 +293,19 @@ class Runner:
         self.lib = N.lib()
         self.cfg = cfg
         self.tree = isinstance(cfg, synth.TreeConfig)
+        self.sample = isinstance(cfg, synth.TreeSampleConfig)
         self.sets = []
         self.keep = []
         vp = lambda t: ctypes.c_void_p(t.data_ptr()) if t is not None else None
-        if self.tree:
+        if self.sample:
+            d = N.TreeSampleDesc()
+            d.batch, d.nodes, d.vocab, d.max_depth = cfg.batch, cfg.nodes, cfg.vocab, cfg.max_depth
+            d.temperature, d.top_p = cfg.temperature, cfg.top_p
+            d.dtype = N.SV_BF16 if cfg.dtype == "bf16" else N.SV_F32
+            d.target_row_stride = d.draft_row_stride = cfg.vocab
+            self.desc = d
+            ws_need = self.lib.sv_tree_sample_workspace_size(ctypes.byref(d))
+        elif self.tree:
             B, Nn = cfg.batch, cfg.nodes
             d = N.TreeDesc()
             d.batch, d.nodes, d.vocab, d.max_depth = B, Nn, cfg.vocab, cfg.max_depth
@@ -306,7 +327,14 @@ class Runner:
                         path=torch.empty((B, L), dtype=torch.int32, device=dev))
         o = self.out
         for s in range(nsets):
-            if self.tree:
+            if self.sample:
+                lg = inputs["logits"] if s == 0 else inputs["logits"].clone()
+                dr = inputs["draft"] if s == 0 else inputs["draft"].clone()
+                self.keep += [lg, dr]
+                args = (ctypes.byref(self.desc), vp(lg), vp(dr), vp(inputs["parents"]), vp(inputs["tokens"]),
+                        vp(inputs["u_accept"]), vp(inputs["u_final"]), vp(o["k"]), vp(o["path"]), vp(o["tokens"]),
+                        vp(o["status"]), vp(self.ws), ctypes.c_size_t(self.ws.numel()))
+            elif self.tree:
                 lg = inputs["logits"] if s == 0 else inputs["logits"].clone()
                 self.keep.append(lg)
                 args = (ctypes.byref(self.desc), vp(lg), vp(inputs["parents"]), vp(inputs["tokens"]),
@@ -325,6 +353,8 @@ class Runner:
             self.sets.append(args)
         self.fn = (self.lib.sv_verify_tree_path if path_walk else self.lib.sv_verify_tree) if self.tree \
             else self.lib.sv_verify_chain
+        if self.sample:
+            self.fn = self.lib.sv_verify_tree_sample
         if topk:
             # Every node row of every tree: R = B*N rows, k ids each.
             kd = N.TopkDesc()
@@ -446,6 +476,10 @@ def run_ours(args, dist: Dist):
     dom_name = {True: "greedy_kernel(tree)", False: None}[R.tree]
     if args.workload in TOPK:
         dom_name = "topk_kernel"
+    if R.sample:
+        # The statistics pass over every target and draft row; the walk reads
+        # only the visited nodes' rows after it.
+        dom_name = "topp_slice_kernel" if cfg.top_p < 1 else "stats_stream_kernel"
     if not R.tree:
         dom_name = "greedy_kernel(chain)" if cfg.temperature == 0 else (
             "topp_slice_kernel" if cfg.top_p < 1 else "stats_stream_kernel")
@@ -494,7 +528,9 @@ def config_of(cfg, workload, nsets, world):
         "not applicable (CPU oracle)"
     c = {"workload": workload, "batch": cfg.batch, "vocab": cfg.vocab, "dtype": cfg.dtype, "l2": l2,
          "parallelism": f"replicas x{world} (batch rows independent)"}
-    if isinstance(cfg, synth.TreeConfig):
+    if isinstance(cfg, synth.TreeSampleConfig):
+        c.update(nodes=cfg.nodes, max_depth=cfg.max_depth, temperature=cfg.temperature, top_p=cfg.top_p)
+    elif isinstance(cfg, synth.TreeConfig):
         c.update(nodes=cfg.nodes, max_depth=cfg.max_depth, temperature=0.0)
     else:
         c.update(gamma=cfg.gamma, temperature=cfg.temperature, top_p=cfg.top_p,
@@ -505,8 +541,11 @@ def config_of(cfg, workload, nsets, world):
 def run_e2e(cfg, inputs, sv, dev, stream, K, dist, path_walk=False, topk=0):
     import torch
     tree = isinstance(cfg, synth.TreeConfig)
+    sample = isinstance(cfg, synth.TreeSampleConfig)
     names = ["logits", "parents", "tokens"] if tree else \
         ["target", "draft", "ids", "u_accept", "u_resample"]
+    if sample:
+        names = ["logits", "draft", "parents", "tokens", "u_accept", "u_final"]
     if topk:
         names = ["logits"]
     if not tree and cfg.temperature == 0:
@@ -527,6 +566,11 @@ def run_e2e(cfg, inputs, sv, dev, stream, K, dist, path_walk=False, topk=0):
         if topk:
             ids = sv.topk(devb["logits"].reshape(cfg.batch * cfg.nodes, cfg.vocab), topk)
             out_host.copy_(ids.reshape(cfg.batch, -1), non_blocking=True)
+        elif sample:
+            o = sv.verify_tree_sample(devb["logits"], devb["draft"], devb["parents"], devb["tokens"],
+                                      devb["u_accept"], devb["u_final"], cfg.max_depth, cfg.temperature, cfg.top_p)
+            out_host.copy_(o["out_tokens"], non_blocking=True)
+            k_host.copy_(o["accept_len"], non_blocking=True)
         elif tree:
             o = sv.verify_tree(devb["logits"], devb["parents"], devb["tokens"], cfg.max_depth, path_walk=path_walk)
             out_host.copy_(o["out_tokens"], non_blocking=True)
@@ -560,6 +604,10 @@ def run_e2e(cfg, inputs, sv, dev, stream, K, dist, path_walk=False, topk=0):
 
 def oracle_rows(cfg, host, rows):
     from oracle import sv_oracle as O
+    if isinstance(cfg, synth.TreeSampleConfig):
+        return O.verify_tree_sample(host["logits"], host["draft_logits"], host["parents"], host["tokens"],
+                                    host["u_accept"], host["u_final"], cfg.temperature, cfg.top_p,
+                                    host["max_depth"], rows=rows)
     if isinstance(cfg, synth.TreeConfig):
         return O.verify_tree(host["logits"], host["parents"], host["tokens"], host["max_depth"], rows=rows)
     return O.verify_chain(host["target"], host["draft"] if cfg.temperature > 0 else None,
@@ -605,7 +653,8 @@ def run_reference(args, dist: Dist):
     of batch rows of the same workload."""
     cfg = WORKLOADS[args.workload]
     chain = not isinstance(cfg, synth.TreeConfig)
-    host = synth.make_chain_inputs(cfg) if chain else synth.make_tree_inputs(cfg)
+    host = synth.make_chain_inputs(cfg) if chain else (
+        synth.make_tree_sample_inputs(cfg) if isinstance(cfg, synth.TreeSampleConfig) else synth.make_tree_inputs(cfg))
     if chain:
         oracle_draft_ids(cfg, host, [0])
     t0 = time.perf_counter()

@@ -6,7 +6,8 @@ marshals PyTorch tensors into its calls.
 """
 from . import _native
 from ._native import SVError, lib
-from .verify import build_t2d, d2t_scatter, sample, softmax_topp, topk, verify_chain, verify_tree, workspace
+from .verify import (build_t2d, d2t_scatter, sample, softmax_topp, topk, verify_chain, verify_tree,
+                     verify_tree_sample, workspace)
 
-__all__ = ["SVError", "lib", "build_t2d", "d2t_scatter", "sample", "softmax_topp", "topk", "verify_chain", "verify_tree",
-           "workspace", "_native"]
+__all__ = ["SVError", "lib", "build_t2d", "d2t_scatter", "sample", "softmax_topp", "topk", "verify_chain",
+           "verify_tree", "verify_tree_sample", "workspace", "_native"]

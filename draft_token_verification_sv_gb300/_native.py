@@ -52,6 +52,13 @@ class SampleDesc(ctypes.Structure):
                 ("row_stride", ctypes.c_int64)]
 
 
+class TreeSampleDesc(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("nodes", ctypes.c_int32), ("vocab", ctypes.c_int32),
+                ("max_depth", ctypes.c_int32), ("temperature", ctypes.c_float), ("top_p", ctypes.c_float),
+                ("dtype", ctypes.c_int32), ("target_row_stride", ctypes.c_int64),
+                ("draft_row_stride", ctypes.c_int64)]
+
+
 class TopkDesc(ctypes.Structure):
     _fields_ = [("rows", ctypes.c_int32), ("vocab", ctypes.c_int32), ("k", ctypes.c_int32),
                 ("dtype", ctypes.c_int32), ("row_stride", ctypes.c_int64)]
@@ -74,6 +81,9 @@ SIGNATURES = {
     "sv_verify_tree": (_I32, [ctypes.POINTER(TreeDesc), _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "sv_tree_path_workspace_size": (_SZ, [ctypes.POINTER(TreeDesc)]),
     "sv_topk": (_I32, [ctypes.POINTER(TopkDesc), _P, _P, _P, _P]),
+    "sv_tree_sample_workspace_size": (_SZ, [ctypes.POINTER(TreeSampleDesc)]),
+    "sv_verify_tree_sample": (_I32, [ctypes.POINTER(TreeSampleDesc), _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                     _P, _SZ, _P]),
     "sv_verify_tree_path": (_I32, [ctypes.POINTER(TreeDesc), _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "sv_d2t_scatter": (_I32, [_P, _I64, _P, _P, _I32, _I32, _I32, _I32, _F, _P, _I64, _P]),
     "sv_build_t2d": (_I32, [_P, _I32, _I32, _P, _P, _P]),

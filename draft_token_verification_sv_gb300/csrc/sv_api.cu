@@ -59,6 +59,20 @@ bool tree_desc_ok(const sv_tree_desc* d) {
   return true;
 }
 
+bool tree_sample_desc_ok(const sv_tree_sample_desc* d) {
+  if (!d) return false;
+  if (d->batch < 0 || d->nodes < 1 || d->nodes > SV_MAX_TREE_NODES) return false;
+  if (d->max_depth < 0 || d->max_depth > SV_MAX_TREE_DEPTH) return false;
+  if (!valid_vocab(d->vocab) || !valid_dtype(d->dtype)) return false;
+  if (!std::isfinite(d->temperature) || !(d->temperature > 0.0f)) return false;
+  if (!(d->top_p > 0.0f && d->top_p <= 1.0f)) return false;
+  if (!valid_stride(d->target_row_stride, d->vocab, d->dtype)) return false;
+  if (!valid_stride(d->draft_row_stride, d->vocab, d->dtype)) return false;
+  // Statistics grid: 2*B*N rows, up to 16 blocks each.
+  if (static_cast<int64_t>(d->batch) * d->nodes * 2 * 16 > INT32_MAX) return false;
+  return true;
+}
+
 bool sample_desc_ok(const sv_sample_desc* d) {
   if (!d) return false;
   if (d->rows < 0 || !valid_vocab(d->vocab) || !valid_dtype(d->dtype)) return false;
@@ -177,6 +191,28 @@ sv_status sv_verify_tree_path(const sv_tree_desc* desc, const void* logits, cons
   if (workspace_bytes < sv_tree_path_workspace_size(desc)) return SV_ERR_WORKSPACE_TOO_SMALL;
   return greedy_tree_walk(*desc, logits, parents, tokens, accept_len, path, out_tokens, row_status,
                           workspace, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t sv_tree_sample_workspace_size(const sv_tree_sample_desc* desc) {
+  if (!tree_sample_desc_ok(desc)) return 0;
+  return tree_sample_workspace_bytes(*desc);
+}
+
+sv_status sv_verify_tree_sample(const sv_tree_sample_desc* desc, const void* target_logits,
+                                const void* draft_logits, const int32_t* parents, const int32_t* tokens,
+                                const float* u_accept, const float* u_final, int32_t* accept_len,
+                                int32_t* path, int32_t* out_tokens, int32_t* row_status,
+                                void* workspace, size_t workspace_bytes, sv_stream_t stream) {
+  CallScope scope;
+  if (!tree_sample_desc_ok(desc)) return SV_ERR_INVALID_ARGUMENT;
+  if (desc->batch == 0) return SV_OK;
+  if (!target_logits || !aligned_elem(target_logits, desc->dtype) || !draft_logits ||
+      !aligned_elem(draft_logits, desc->dtype) || !parents || !tokens || !u_accept || !u_final ||
+      !accept_len || !path || !out_tokens || !workspace)
+    return SV_ERR_INVALID_ARGUMENT;
+  if (workspace_bytes < sv_tree_sample_workspace_size(desc)) return SV_ERR_WORKSPACE_TOO_SMALL;
+  return tree_sample(*desc, target_logits, draft_logits, parents, tokens, u_accept, u_final, accept_len, path,
+                     out_tokens, row_status, workspace, reinterpret_cast<cudaStream_t>(stream));
 }
 
 sv_status sv_topk(const sv_topk_desc* desc, const void* logits, int32_t* out_ids, float* out_vals,

@@ -138,7 +138,7 @@ static sv_status launch_stream(const StatsLaunch& L, int rows, cudaStream_t stre
 
 // One launch when both row sets share a dtype, else one per set.  top_p < 1
 // selects the top-p kernel, whose scratch follows the row statistics.
-static sv_status launch_stats_sets(StatsLaunch L, sv_dtype d0, sv_dtype d1, bool topp, void* scratch,
+sv_status launch_stats_sets(StatsLaunch L, sv_dtype d0, sv_dtype d1, bool topp, void* scratch,
                                    cudaStream_t stream) {
   auto one = [&](const StatsLaunch& X, sv_dtype dt, void* scr) -> sv_status {
     if (topp) return launch_topp_stats(X, dt, scr, stream);

@@ -92,6 +92,12 @@ sv_status greedy_tree(const sv_tree_desc& d, const void* logits, const int32_t* 
                       cudaStream_t stream);
 sv_status greedy_sample(const sv_sample_desc& d, const void* logits, int32_t* out_tokens,
                         float* out_prob, cudaStream_t stream);
+// Speculative-sampling tree verify (sv_tree_sample.cu).
+size_t tree_sample_workspace_bytes(const sv_tree_sample_desc& d);
+sv_status tree_sample(const sv_tree_sample_desc& d, const void* target, const void* draft,
+                      const int32_t* parents, const int32_t* tokens, const float* u_accept,
+                      const float* u_final, int32_t* accept_len, int32_t* path, int32_t* out_tokens,
+                      int32_t* row_status, void* workspace, cudaStream_t stream);
 // Top-k ids per row (sv_topk.cu).
 sv_status topk_rows(const sv_topk_desc& d, const void* logits, int32_t* out_ids, float* out_vals,
                     cudaStream_t stream);

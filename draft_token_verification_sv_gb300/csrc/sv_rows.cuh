@@ -220,5 +220,9 @@ sv_status launch_decide(const DecideParams& P, sv_dtype target_dtype, sv_dtype d
 // Top-p statistics of every row of L (sv_topp.cu), with `scratch` of
 // topp_scratch_bytes(...) bytes (slice summaries and row counters).
 sv_status launch_topp_stats(StatsLaunch L, sv_dtype dtype, void* scratch, cudaStream_t stream);
+// Statistics of one or two row sets (sv_chain.cu): the streaming kernel, or
+// the top-p kernel when `topp`, with its scratch at `scratch`.
+sv_status launch_stats_sets(StatsLaunch L, sv_dtype d0, sv_dtype d1, bool topp, void* scratch,
+                            cudaStream_t stream);
 
 }  // namespace sv

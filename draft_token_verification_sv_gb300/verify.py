@@ -178,6 +178,51 @@ def verify_tree(logits: torch.Tensor, parents: torch.Tensor, tokens: torch.Tenso
     return out
 
 
+def verify_tree_sample(target_logits: torch.Tensor, draft_logits: torch.Tensor, parents: torch.Tensor,
+                       tokens: torch.Tensor, u_accept: torch.Tensor, u_final: torch.Tensor, max_depth: int,
+                       temperature: float, top_p: float = 1.0, *, out: dict | None = None,
+                       ws: torch.Tensor | None = None, stream=None) -> dict:
+    """Speculative-sampling verify of B draft trees (T > 0); see
+    sv_verify_tree_sample.
+
+    target_logits / draft_logits [B, N, V] (same dtype), parents/tokens [B, N]
+    int32, u_accept [B, N] and u_final [B] float32.  Returns dict(accept_len
+    [B], path [B, D+1], out_tokens [B, D+1], row_status [B]).
+    """
+    for t, n in ((target_logits, "target_logits"), (draft_logits, "draft_logits"), (parents, "parents"),
+                 (tokens, "tokens"), (u_accept, "u_accept"), (u_final, "u_final")):
+        _cuda(t, n)
+    B, Nn, V = target_logits.shape
+    if tuple(draft_logits.shape) != (B, Nn, V) or draft_logits.dtype != target_logits.dtype:
+        raise ValueError("draft_logits must match target_logits in shape and dtype")
+    d = N.TreeSampleDesc()
+    d.batch, d.nodes, d.vocab, d.max_depth = B, Nn, V, int(max_depth)
+    d.temperature, d.top_p = float(temperature), float(top_p)
+    d.dtype = _code(target_logits)
+    d.target_row_stride = _row_stride(target_logits, "target_logits")
+    d.draft_row_stride = _row_stride(draft_logits, "draft_logits")
+    dev = target_logits.device
+    L = int(max_depth) + 1
+    if out is None:
+        out = dict(accept_len=torch.empty(B, dtype=torch.int32, device=dev),
+                   path=torch.empty((B, L), dtype=torch.int32, device=dev),
+                   out_tokens=torch.empty((B, L), dtype=torch.int32, device=dev),
+                   row_status=torch.empty(B, dtype=torch.int32, device=dev))
+    lib = N.lib()
+    need = lib.sv_tree_sample_workspace_size(ctypes.byref(d))
+    if need == 0:
+        raise ValueError("invalid tree sampling descriptor")
+    if ws is None:
+        ws = workspace(need, dev, stream)
+    st = lib.sv_verify_tree_sample(
+        ctypes.byref(d), _p(target_logits), _p(draft_logits), _p(_i32(parents, "parents")),
+        _p(_i32(tokens, "tokens")), _p(_f32(u_accept, "u_accept")), _p(_f32(u_final, "u_final")),
+        _p(out["accept_len"]), _p(out["path"]), _p(out["out_tokens"]), _p(out.get("row_status")), _p(ws),
+        ctypes.c_size_t(ws.numel()), _stream(stream))
+    N.check(st, "sv_verify_tree_sample")
+    return out
+
+
 def topk(logits: torch.Tensor, k: int, *, values: bool = False, stream=None):
     """Top-k node expansion; see sv_topk.  logits [R, V] -> ids [R, k] int32
     (and their logits [R, k] float32 when ``values``)."""

@@ -232,6 +232,60 @@ sv_status sv_verify_tree_path(const sv_tree_desc* desc, const void* logits,
                               int32_t* row_status, void* workspace, size_t workspace_bytes,
                               sv_stream_t stream);
 
+typedef struct sv_tree_sample_desc {
+  int32_t batch;             /* B >= 0 trees */
+  int32_t nodes;             /* N in [1, SV_MAX_TREE_NODES] nodes per tree, node 0 = root */
+  int32_t vocab;             /* V in [1, SV_MAX_VOCAB], shared by target and draft rows */
+  int32_t max_depth;         /* D in [0, SV_MAX_TREE_DEPTH] */
+  float temperature;         /* T > 0 */
+  float top_p;               /* in (0, 1]; 1 = no filtering */
+  sv_dtype dtype;            /* of both logits arrays */
+  int64_t target_row_stride; /* elements between consecutive node rows (>= V) */
+  int64_t draft_row_stride;
+} sv_tree_sample_desc;
+
+/* Workspace bytes for sv_verify_tree_sample (scratch, no initialisation);
+ * 0 for an invalid descriptor. */
+size_t sv_tree_sample_workspace_size(const sv_tree_sample_desc* desc);
+
+/*
+ * Speculative-sampling verify of B draft token trees at T > 0 ([P2] §5 tree;
+ * [P3] §3.1 accept rule, §6.2 shared T and top_p).  The pages give no rule
+ * for several drafts at one position; this call uses sequential per-child
+ * rejection with a residual update.  At an accepted node, with
+ * p = dist(target row), q = dist(draft row) (softmax of top_p_filter(l / T),
+ * as in sv_verify_chain), the residual r starts as p; the node's children
+ * are tested in increasing node order: a child with token x is accepted iff
+ * u_accept[child] * q(x) < r(x); a rejection replaces r by
+ * norm(max(0, r - q)) (when that has no mass -- impossible in exact
+ * arithmetic for a token the draft could have drawn -- r is kept and
+ * SV_ROW_RESAMPLE_FALLBACK is set).  The first accepted child becomes the
+ * node.  When every child is rejected the last token is drawn from r, at a
+ * node without children from p, by inverse CDF with u_final (first id whose
+ * inclusive prefix exceeds u * total).  The emitted tokens follow the
+ * target when each node's children are independent draws from its q.
+ *
+ *   target_logits [B, N] rows of V elements (row b*N+n: the target at node n).
+ *   draft_logits  [B, N] rows of V elements (the draft at node n, which the
+ *                 children of n were drawn from; rows of leaves are read only
+ *                 by the statistics pass).
+ *   parents, tokens [B, N] int32 as for sv_verify_tree.
+ *   u_accept      [B, N] float in [0, 1): the accept uniform of each node (n = 0 unused).
+ *   u_final       [B] float in [0, 1).
+ *   accept_len    [B] int32: depth of the last accepted node.
+ *   path          [B, D+1] int32: node ids from the root, -1 padded.
+ *   out_tokens    [B, D+1] int32: accepted tokens then the drawn token, -1 padded.
+ *   row_status    optional [B] int32 (SV_ROW_*): invalid trees and trees with a
+ *                 row of no finite logit emit nothing (accept_len 0, -1s).
+ *
+ * Launches: the row statistics of all 2*B*N rows, then one block per tree.
+ */
+sv_status sv_verify_tree_sample(const sv_tree_sample_desc* desc, const void* target_logits,
+                                const void* draft_logits, const int32_t* parents, const int32_t* tokens,
+                                const float* u_accept, const float* u_final, int32_t* accept_len,
+                                int32_t* path, int32_t* out_tokens, int32_t* row_status,
+                                void* workspace, size_t workspace_bytes, sv_stream_t stream);
+
 /*
  * Top-k node expansion for building a draft token tree ([P2] §5: every node
  * grows into its top_k draft tokens): the k ids with the highest logits of

@@ -90,6 +90,17 @@ class TreeConfig:
         return self.batch * self.nodes * self.vocab * self.esize()
 
 
+@dataclasses.dataclass(frozen=True)
+class TreeSampleConfig(TreeConfig):
+    """A tree workload verified by speculative sampling at temperature T and
+    top_p: target and draft logits at every node."""
+    temperature: float = 1.0
+    top_p: float = 1.0
+
+    def algorithmic_bytes(self) -> int:
+        return 2 * super().algorithmic_bytes()  # target and draft rows
+
+
 TINY = ChainConfig("tiny", 1, 3, 1000, "f32", 0.8, 0.9, 2.0, 0.5, number=1)
 SMOLLM2 = ChainConfig("smollm2", 64, 5, 49152, "bf16", 0.8, 0.9, 3.0, 0.7,
                       spikes=5, spike_value=8.0, number=2)
@@ -98,6 +109,8 @@ LLAMA3_SAMPLE = ChainConfig("llama3-sample", 128, 6, 128256, "bf16", 1.0, 1.0, 2
 QWEN3_D2T = ChainConfig("qwen3-d2t", 256, 7, 151936, "f32", 1.0, 0.95, 2.0, 0.7,
                         draft_vocab=32000, number=4)
 TREE = TreeConfig("tree", 64, 32, 128256, "bf16", 5, 8, 2.0, 0.7, 16.0, number=5)
+TREE_SAMPLE = TreeSampleConfig("tree-sample", 64, 32, 128256, "bf16", 5, 8, 2.0, 0.7, 16.0, number=5,
+                               temperature=1.0, top_p=1.0)
 
 CHAIN_CONFIGS = {c.name: c for c in (TINY, SMOLLM2, LLAMA3_GREEDY, LLAMA3_SAMPLE, QWEN3_D2T)}
 ALL_CONFIGS = dict(CHAIN_CONFIGS, tree=TREE)
@@ -235,3 +248,24 @@ def make_tree_inputs(cfg: TreeConfig, seed: int | None = None, *, batch: int | N
     values, store = _finish(logits, cfg.dtype)
     return dict(cfg=cfg, seed=seed, batch=B, nodes=N, vocab=V, logits=values,
                 logits_store=store, parents=parents, tokens=tokens, max_depth=cfg.max_depth)
+
+
+def make_tree_sample_inputs(cfg: TreeConfig, seed: int | None = None, *, batch: int | None = None,
+                            vocab: int | None = None, nodes: int | None = None,
+                            draft_noise: float = 1.0) -> dict:
+    """The tree workload plus what sampling verify needs.
+
+    draft_logits [B, N, V]: the target logits plus seeded Gaussian noise of
+    scale ``draft_noise`` (a draft that shares the target's planted peaks and
+    differs from it everywhere else); u_accept [B, N] and u_final [B] fp32
+    uniforms in [0, 1).  The children are the tree workload's tokens (the
+    planted child first), not draws from the draft.
+    """
+    tr = make_tree_inputs(cfg, seed, batch=batch, vocab=vocab, nodes=nodes)
+    g_d, g_u = rng(tr["seed"], 7), rng(tr["seed"], 8)
+    draft = tr["logits"] + g_d.normal(0.0, draft_noise, size=tr["logits"].shape).astype(np.float32)
+    dvals, dstore = _finish(draft, cfg.dtype)
+    B, N = tr["batch"], tr["nodes"]
+    tr.update(draft_logits=dvals, draft_store=dstore,
+              u_accept=g_u.random((B, N), dtype=np.float32), u_final=g_u.random(B, dtype=np.float32))
+    return tr

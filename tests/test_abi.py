@@ -255,3 +255,38 @@ def test_tree_path_pointer_and_workspace_checks(N):
     assert f(ctypes.byref(d), None, A, A, A, A, A, None, A, ctypes.c_size_t(need), None) == 1
     assert f(ctypes.byref(d), A, A, A, A, A, A, None, A, ctypes.c_size_t(need - 1), None) == 4
     assert f(ctypes.byref(_tree(N, nodes=0)), A, A, A, A, A, A, None, A, ctypes.c_size_t(need), None) == 1
+
+
+def _tsample(N, **kw):
+    d = N.TreeSampleDesc()
+    d.batch, d.nodes, d.vocab, d.max_depth = 2, 32, 1000, 5
+    d.temperature, d.top_p, d.dtype = 1.0, 1.0, N.SV_BF16
+    d.target_row_stride, d.draft_row_stride = 1000, 1000
+    for k, v in kw.items():
+        setattr(d, k, v)
+    return d
+
+
+@pytest.mark.parametrize("field,value", [("temperature", 0.0), ("temperature", -1.0), ("top_p", 0.0),
+                                         ("top_p", 1.5), ("nodes", 0), ("nodes", 1025), ("max_depth", 65),
+                                         ("draft_row_stride", 999), ("vocab", 0)])
+def test_tree_sample_rejects_bad_descriptor(N, field, value):
+    d = _tsample(N, **{field: value})
+    assert N.lib().sv_tree_sample_workspace_size(ctypes.byref(d)) == 0
+    f = N.lib().sv_verify_tree_sample
+    assert f(ctypes.byref(d), A, A, A, A, A, A, A, A, A, None, A, ctypes.c_size_t(1 << 30), None) == 1
+
+
+def test_tree_sample_pointer_and_workspace_checks(N):
+    d = _tsample(N)
+    need = N.lib().sv_tree_sample_workspace_size(ctypes.byref(d))
+    assert need >= 2 * 2 * 32 * 32                      # target and draft row statistics
+    assert N.lib().sv_tree_sample_workspace_size(ctypes.byref(_tsample(N, top_p=0.9))) > need
+    f = N.lib().sv_verify_tree_sample
+    sz = ctypes.c_size_t(need)
+    assert f(ctypes.byref(d), None, A, A, A, A, A, A, A, A, None, A, sz, None) == 1
+    assert f(ctypes.byref(d), A, MIS, A, A, A, A, A, A, A, None, A, sz, None) == 1
+    assert f(ctypes.byref(d), A, A, A, A, None, A, A, A, A, None, A, sz, None) == 1
+    assert f(ctypes.byref(d), A, A, A, A, A, A, A, A, A, None, A, ctypes.c_size_t(need - 1), None) == 4
+    assert f(ctypes.byref(_tsample(N, batch=0)), None, None, None, None, None, None, None, None, None, None,
+             None, ctypes.c_size_t(0), None) == 0
