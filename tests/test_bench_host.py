@@ -1,0 +1,58 @@
+"""Host logic of bench.py that needs no GPU: every workload's byte count
+and config line, the oracle arm on small copies of each workload (including
+tree sampling), and the seeded inputs being reproducible."""
+import dataclasses
+import os
+import sys
+
+import numpy as np
+import pytest
+
+import synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+def test_every_workload_has_bytes_and_a_config_line():
+    for name, cfg in bench.WORKLOADS.items():
+        b = bench.step_bytes(cfg)
+        assert b > 0
+        c = bench.config_of(cfg, name, bench.n_sets_for(cfg), 1)
+        assert c["workload"] == name and c["batch"] == cfg.batch and c["vocab"] == cfg.vocab
+        assert bench.n_sets_for(cfg) * b > 4 * bench.L2_BYTES      # rotation exceeds 4x L2
+
+
+def test_tree_sample_counts_target_and_draft_rows():
+    s, t = synth.TREE_SAMPLE, synth.TREE
+    assert s.algorithmic_bytes() == 2 * t.algorithmic_bytes() == 2 * 64 * 32 * 128256 * 2
+    c = bench.config_of(s, "tree-sample", 2, 1)
+    assert (c["temperature"], c["top_p"], c["nodes"], c["max_depth"]) == (1.0, 1.0, 32, 5)
+    assert bench.config_of(t, "tree", 2, 1)["temperature"] == 0.0
+
+
+def test_tree_sample_inputs_are_seeded():
+    small = dataclasses.replace(synth.TREE_SAMPLE, batch=2, vocab=300)
+    a = synth.make_tree_sample_inputs(small)
+    b = synth.make_tree_sample_inputs(small)
+    for k in ("logits", "draft_logits", "parents", "tokens", "u_accept", "u_final"):
+        assert np.array_equal(a[k], b[k]), k
+    assert not np.array_equal(a["logits"], a["draft_logits"])
+    assert a["u_accept"].dtype == np.float32 and (0 <= a["u_accept"]).all() and (a["u_accept"] < 1).all()
+    # the same target logits as the greedy tree workload of that shape
+    g = synth.make_tree_inputs(dataclasses.replace(synth.TREE, batch=2, vocab=300))
+    assert np.array_equal(a["logits"], g["logits"]) and np.array_equal(a["tokens"], g["tokens"])
+
+
+@pytest.mark.parametrize("name", ["tree", "tree-sample"])
+def test_oracle_arm_on_small_trees(name):
+    cfg = dataclasses.replace(bench.WORKLOADS[name], batch=3, vocab=500)
+    host = synth.make_tree_sample_inputs(cfg) if isinstance(cfg, synth.TreeSampleConfig) \
+        else synth.make_tree_inputs(cfg)
+    out = bench.oracle_rows(cfg, host, [0, 2])
+    assert out["accept_len"][1] == 0 and np.all(out["out_tokens"][1] == -1)   # row 1 not computed
+    for b in (0, 2):
+        d = out["accept_len"][b]
+        assert 0 <= d <= cfg.max_depth and out["out_tokens"][b][d] >= 0
+    assert bench.units_per_batch_row(cfg) == cfg.nodes
