@@ -517,8 +517,20 @@ def run_ours(args, dist: Dist):
         "e2e": e2e,
         "clocks": clocks,
     }
+    if args.workload not in TOPK:
+        # Accepted drafts per batch row in the last replayed step.
+        try:
+            res["mean_accepted"] = float(R.out["k"].float().mean().item())
+        except Exception:
+            res["mean_accepted"] = None
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
-        res["cpu_baseline"] = cpu_baseline(cfg, inputs, args.cpu_seconds)
+        sampled = []
+        res["cpu_baseline"] = cpu_baseline(cfg, inputs, args.cpu_seconds, sink=sampled)
+        if args.workload not in TOPK:
+            try:
+                res["parity_sample"] = parity_sample(cfg, sampled, R.out["tokens"].cpu().numpy())
+            except Exception as e:  # never let the cross-check cost the measurement
+                res["parity_sample"] = {"error": str(e)[:200]}
     dist.close()
     return res
 
@@ -619,19 +631,42 @@ def units_per_batch_row(cfg) -> int:
     return cfg.nodes if isinstance(cfg, synth.TreeConfig) else 2 * cfg.gamma + 1
 
 
-def cpu_baseline(cfg, inputs, seconds):
+def cpu_baseline(cfg, inputs, seconds, sink=None):
     """The fp64 oracle as it stands, single-threaded, on batch rows of the
-    same workload until the CPU budget is spent (at least one row)."""
+    same workload until the CPU budget is spent (at least one row).  Each
+    row's oracle output is appended to ``sink`` as (row, output)."""
     host = inputs["host"]
     B = cfg.batch
     done = 0
     t0 = time.perf_counter()
     while done < B and (done == 0 or time.perf_counter() - t0 < seconds):
-        oracle_rows(cfg, host, [done])
+        out = oracle_rows(cfg, host, [done])
+        if sink is not None:
+            sink.append((done, out))
         done += 1
     dt = time.perf_counter() - t0
     return {"value": done * units_per_batch_row(cfg) / dt, "unit": "rows/s", "cores": 1, "kind": "oracle",
             "sample": f"{done} of {B} batch rows of the {cfg.name} workload, fp64 numpy, one thread"}
+
+
+def parity_sample(cfg, sampled, got_tokens) -> dict:
+    """The batch rows the oracle computed for the CPU baseline against the
+    library's tokens for the same rows of the timed workload: how many rows
+    differ, and how many of those have an oracle decision within the
+    near-threshold margin (1e-6 in the uniform's units; 1e-5 for tree
+    sampling, whose accept tests divide by a residual mass summed in fp32)."""
+    from oracle import sv_oracle as O
+    tree = isinstance(cfg, synth.TreeConfig)
+    tol = 1e-5 if isinstance(cfg, synth.TreeSampleConfig) else O.NEAR
+    mismatch = near = 0
+    for b, out in sampled:
+        want = out["out_tokens"][b] if tree else out["tokens"][b]
+        if not np.array_equal(np.asarray(got_tokens[b], dtype=np.int64), np.asarray(want, dtype=np.int64)):
+            mismatch += 1
+            margin = out.get("margin")
+            if margin is not None and margin[b] < tol:
+                near += 1
+    return {"rows": len(sampled), "mismatch": mismatch, "near_threshold": near}
 
 
 def oracle_draft_ids(cfg, host, rows):

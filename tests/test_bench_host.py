@@ -56,3 +56,28 @@ def test_oracle_arm_on_small_trees(name):
         d = out["accept_len"][b]
         assert 0 <= d <= cfg.max_depth and out["out_tokens"][b][d] >= 0
     assert bench.units_per_batch_row(cfg) == cfg.nodes
+
+
+@pytest.mark.parametrize("name", ["tiny", "tree", "tree-sample"])
+def test_parity_sample_counts_mismatches(name):
+    cfg = bench.WORKLOADS[name]
+    if isinstance(cfg, synth.TreeConfig):
+        cfg = dataclasses.replace(cfg, batch=4, vocab=400)
+        host = synth.make_tree_sample_inputs(cfg) if isinstance(cfg, synth.TreeSampleConfig) \
+            else synth.make_tree_inputs(cfg)
+        key = "out_tokens"
+    else:
+        host = synth.make_chain_inputs(cfg, batch=4)
+        bench.oracle_draft_ids(cfg, host, range(4))
+        key = "tokens"
+    sampled = []
+    inputs = {"host": host}
+    cfg_b = dataclasses.replace(cfg, batch=4)
+    base = bench.cpu_baseline(cfg_b, inputs, 0.0, sink=sampled)
+    assert base["kind"] == "oracle" and len(sampled) >= 1
+    got = np.stack([out[key][b] for b, out in sampled] + [np.full_like(sampled[0][1][key][0], -1)] * 4)
+    assert bench.parity_sample(cfg_b, sampled, got) == {"rows": len(sampled), "mismatch": 0,
+                                                        "near_threshold": 0}
+    got[0, 0] = got[0, 0] + 1
+    r = bench.parity_sample(cfg_b, sampled, got)
+    assert r["mismatch"] == 1 and r["near_threshold"] in (0, 1)
