@@ -301,6 +301,8 @@ __global__ void __launch_bounds__(kTSThreads) tree_sample_kernel(TreeSampleParam
   const E* dft = static_cast<const E*>(P.draft);
   int node = 0, d = 0;
   if (threadIdx.x == 0) path[0] = 0;
+  // Every iteration either moves one level down (parents[n] < n and depths
+  // <= D were checked above) or returns: at most D + 1 iterations.
   for (;;) {
     const int64_t row = base + node;
     if (threadIdx.x < 2) {
