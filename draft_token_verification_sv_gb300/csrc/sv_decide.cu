@@ -445,15 +445,16 @@ static sv_status launch_decide_typed(DecideParams P, void* scratch, cudaStream_t
 // the launch about four blocks per SM; fewer chunks per block otherwise, so
 // small batches still spread over the GPU.
 static int chunks_per_block(int B, int V, int nc_max) {
-  static int sms[64] = {};
+  // SM count per device, cached; concurrent callers store the same value.
+  static std::atomic<int> sms[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
-  if (sms[dev] == 0) {
-    int n = 0;
+  int n = sms[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
-    sms[dev] = n;
+    sms[dev].store(n, std::memory_order_relaxed);
   }
-  const long long want = 4LL * sms[dev];
+  const long long want = 4LL * n;
   const int nchunks = (V + kDChunk - 1) / kDChunk;
   int nc = nc_max;
   while (nc > 2 && static_cast<long long>(B) * ((nchunks + nc - 1) / nc) < want) nc /= 2;

@@ -50,6 +50,11 @@ sv_status sv_verify_chain_static(const sv_chain_desc* desc, const void* target_l
                                  const int32_t* draft_ids, const float* u_accept, const float* u_resample,
                                  int32_t* out_tokens, int32_t* num_accepted, float* p_draft, float* q_draft,
                                  int32_t* row_status, sv_stream_t stream) {
+  // An empty batch needs no scratch: sv_verify_chain checks the descriptor
+  // and returns without touching the device.
+  if (desc && desc->batch == 0)
+    return sv_verify_chain(desc, target_logits, draft_logits, d2t, t2d, draft_ids, u_accept, u_resample,
+                           out_tokens, num_accepted, p_draft, q_draft, row_status, nullptr, 0, stream);
   const size_t need = sv_chain_workspace_size(desc);
   if (need == 0) return SV_ERR_INVALID_ARGUMENT;
   if (need > kStaticScratchBytes) return SV_ERR_WORKSPACE_TOO_SMALL;

@@ -156,7 +156,12 @@ sv_status sv_verify_chain(const sv_chain_desc* desc,
  *     with SV_ERR_WORKSPACE_TOO_SMALL before anything runs.
  *   - The first call on a device looks up the array's device address (with
  *     that device current) and caches it; make that first call outside any
- *     stream capture.
+ *     stream capture.  The cached address belongs to the device's context as
+ *     it was then: after cudaDeviceReset on that device the address is stale,
+ *     so a process that resets a device must not call this entry point on it
+ *     again (restart the process instead).
+ *   - An empty batch (desc->batch == 0) is checked like sv_verify_chain
+ *     checks it and returns SV_OK without touching the device.
  *   - All calls on a device share the one array, which keeps whatever the
  *     last call left in it.  The verify path needs no zeroed scratch (it
  *     clears its own counters on every call).  Calls that may overlap on the

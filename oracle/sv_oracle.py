@@ -240,6 +240,11 @@ def verify_chain_row(target_logits: np.ndarray, draft_logits: np.ndarray | None,
 
     Returns dict(tokens [γ+1] int64 (-1 padded), k, p_draft [γ], q_draft [γ],
     margin (smallest decision margin on the path that produced the output),
+    near_from (the first output position decided by a decision whose margin
+    is below NEAR -- the top-p cut of row i or the accept test of draft i
+    decide position i, the draw decides position k --; γ+1 when none),
+    pq_margin [γ+1, 2] (top-p margins of target row i and draft row i, for
+    every row whose distribution was computed; inf otherwise),
     status, resample_fallback (bool: residual mass was 0)).
     """
     target_logits = np.asarray(target_logits, dtype=np.float64)
@@ -248,7 +253,8 @@ def verify_chain_row(target_logits: np.ndarray, draft_logits: np.ndarray | None,
     ids = np.asarray(draft_ids, dtype=np.int64)
     tokens = np.full(gamma + 1, -1, dtype=np.int64)
     res = dict(tokens=tokens, k=0, p_draft=np.zeros(gamma), q_draft=np.zeros(gamma),
-               margin=np.inf, status=0, resample_fallback=False)
+               margin=np.inf, near_from=gamma + 1, pq_margin=np.full((gamma + 1, 2), np.inf),
+               status=0, resample_fallback=False)
 
     if np.any((ids < 0) | (ids >= vocab)):
         res["status"] = STATUS_BAD_DRAFT_ID
@@ -273,11 +279,14 @@ def verify_chain_row(target_logits: np.ndarray, draft_logits: np.ndarray | None,
     if not np.all(np.any(np.isfinite(draft_logits), axis=1)):
         res["status"] = STATUS_EMPTY_ROW
         return res
-    margins = []
+    margins = []   # margin of every decision on the output's path
+    decides = []   # the output position each of those decisions decides
 
     def p_row(i):
         p, mg = dist(target_logits[i], temperature, top_p)
         margins.append(mg)
+        decides.append(i)
+        res["pq_margin"][i, 0] = mg
         return p
 
     def q_row(i):
@@ -287,6 +296,8 @@ def verify_chain_row(target_logits: np.ndarray, draft_logits: np.ndarray | None,
             scattered = d2t_scatter(draft_logits[i], d2t, vocab)[0]
             q, mg = dist(scattered, temperature, top_p)
         margins.append(mg)
+        decides.append(i)
+        res["pq_margin"][i, 1] = mg
         return q
 
     k = gamma
@@ -299,6 +310,7 @@ def verify_chain_row(target_logits: np.ndarray, draft_logits: np.ndarray | None,
         accept = u_accept[i] * q_i[x] < p_i[x]
         if q_i[x] > 0.0:
             margins.append(abs(float(u_accept[i]) - p_i[x] / q_i[x]))
+            decides.append(i)
         if not accept:
             k = i
             p_k, q_k = p_i, q_i
@@ -307,13 +319,14 @@ def verify_chain_row(target_logits: np.ndarray, draft_logits: np.ndarray | None,
         # The remaining positions are still scored by the target ([P3] §4.2
         # computes every position before deciding); record p/q for them.
         for i in range(k + 1, gamma):
-            p_i, _ = dist(target_logits[i], temperature, top_p)
+            p_i, mg_p = dist(target_logits[i], temperature, top_p)
             if d2t is None:
-                q_i, _ = dist(draft_logits[i], temperature, top_p)
+                q_i, mg_q = dist(draft_logits[i], temperature, top_p)
             else:
-                q_i, _ = dist(d2t_scatter(draft_logits[i], d2t, vocab)[0], temperature, top_p)
+                q_i, mg_q = dist(d2t_scatter(draft_logits[i], d2t, vocab)[0], temperature, top_p)
             res["p_draft"][i] = p_i[ids[i]]
             res["q_draft"][i] = q_i[ids[i]]
+            res["pq_margin"][i] = (mg_p, mg_q)
         residual = np.maximum(0.0, p_k - q_k)   # norm(max(0, p - q)), [P3] §3.1
         if residual.sum() > 0.0:
             tok, mg = inverse_cdf(residual, float(u_resample))
@@ -324,10 +337,13 @@ def verify_chain_row(target_logits: np.ndarray, draft_logits: np.ndarray | None,
         p_g = p_row(gamma)                      # bonus token from p_γ, [P3] §3.1
         tok, mg = inverse_cdf(p_g, float(u_resample))
     margins.append(mg)
+    decides.append(k)
     tokens[:k] = ids[:k]
     tokens[k] = tok
     res["k"] = k
     res["margin"] = float(min(margins)) if margins else np.inf
+    near = [pos for mg_, pos in zip(margins, decides) if mg_ < NEAR]
+    res["near_from"] = min(near) if near else gamma + 1
     return res
 
 
@@ -345,7 +361,8 @@ def verify_chain(target_logits, draft_logits, draft_ids, u_accept, u_resample,
     rows = range(B) if rows is None else rows
     out = dict(tokens=np.full((B, gp1), -1, np.int64), num_accepted=np.zeros(B, np.int64),
                p_draft=np.zeros((B, gamma)), q_draft=np.zeros((B, gamma)),
-               margin=np.full(B, np.inf), status=np.zeros(B, np.int64),
+               margin=np.full(B, np.inf), near_from=np.full(B, gp1, np.int64),
+               pq_margin=np.full((B, gp1, 2), np.inf), status=np.zeros(B, np.int64),
                resample_fallback=np.zeros(B, bool))
     for b in rows:
         r = verify_chain_row(
@@ -358,6 +375,8 @@ def verify_chain(target_logits, draft_logits, draft_ids, u_accept, u_resample,
         out["p_draft"][b] = r["p_draft"]
         out["q_draft"][b] = r["q_draft"]
         out["margin"][b] = r["margin"]
+        out["near_from"][b] = r["near_from"]
+        out["pq_margin"][b] = r["pq_margin"]
         out["status"][b] = r["status"]
         out["resample_fallback"][b] = r["resample_fallback"]
     return out

@@ -73,11 +73,23 @@ def test_parity_sample_counts_mismatches(name):
     sampled = []
     inputs = {"host": host}
     cfg_b = dataclasses.replace(cfg, batch=4)
-    base = bench.cpu_baseline(cfg_b, inputs, 0.0, sink=sampled)
-    assert base["kind"] == "oracle" and len(sampled) >= 1
-    got = np.stack([out[key][b] for b, out in sampled] + [np.full_like(sampled[0][1][key][0], -1)] * 4)
+    base = bench.cpu_baseline(cfg_b, inputs, 0.0, sink=sampled, cores=2)
+    assert base["kind"] == "oracle" and base["cores"] == 2 and len(sampled) >= 1
+    # the workers' rows are the oracle's own rows
+    rows = [b for b, _, _ in sampled]
+    direct = bench.oracle_rows(cfg_b, host, rows)
+    for b, tok, margin in sampled:
+        assert np.array_equal(tok, direct[key][b])
+    got = np.full((4, sampled[0][1].size), -1, np.int64)
+    for b, tok, _ in sampled:
+        got[b] = tok
     assert bench.parity_sample(cfg_b, sampled, got) == {"rows": len(sampled), "mismatch": 0,
                                                         "near_threshold": 0}
-    got[0, 0] = got[0, 0] + 1
+    b0 = sampled[0][0]
+    got[b0, 0] = got[b0, 0] + 1
     r = bench.parity_sample(cfg_b, sampled, got)
     assert r["mismatch"] == 1 and r["near_threshold"] in (0, 1)
+
+
+def test_host_cores_is_positive():
+    assert bench.host_cores() >= 1

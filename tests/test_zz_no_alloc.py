@@ -96,3 +96,23 @@ def test_static_rejects_oversized_requests(sv):
     A = ctypes.c_void_p(0x100000)
     st = lib.sv_verify_chain_static(ctypes.byref(d), A, A, None, None, A, A, A, A, A, None, None, None, None)
     assert st == N.SV_ERR_WORKSPACE_TOO_SMALL
+
+
+@pytest.mark.parametrize("temperature", [0.0, 1.0])
+def test_static_empty_batch(sv, temperature):
+    """An empty batch is a valid call that needs no scratch: SV_OK, as from
+    sv_verify_chain, with nothing launched."""
+    from draft_token_verification_sv_gb300 import _native as N
+    lib = N.lib()
+    d = N.ChainDesc()
+    d.batch, d.gamma, d.vocab, d.draft_vocab = 0, 4, 1000, 1000
+    d.target_dtype = d.draft_dtype = N.SV_F32
+    d.temperature, d.top_p = temperature, 1.0
+    d.target_row_stride = d.draft_row_stride = 1000
+    st = lib.sv_verify_chain_static(ctypes.byref(d), None, None, None, None, None, None, None, None, None,
+                                    None, None, None, None)
+    assert st == N.SV_OK
+    d.top_p = 0.0  # still checked: an invalid descriptor is rejected
+    st = lib.sv_verify_chain_static(ctypes.byref(d), None, None, None, None, None, None, None, None, None,
+                                    None, None, None, None)
+    assert st == N.SV_ERR_INVALID_ARGUMENT
