@@ -60,6 +60,12 @@ constexpr int kMaxStaged = kCandCap / 2;         // slice headers staged in shar
 constexpr int kRegion = kCandCap / (kSThreads / 32);  // candidates per warp in the rescan
 constexpr int kWarps = kSThreads / 32;
 constexpr float kFixCand = 524288.0f;           // 2^19: candidate level masses
+// Magic constants of the FP32-pipe floor and rounding: x + 1.5 * 2^23 holds
+// an integer n in its low mantissa bits for |n| < 2^22 (0x4B400000 + n).
+constexpr float kMagicFloor = 12582912.0f;  // 1.5 * 2^23
+constexpr uint32_t kMagicFloorBits = 0x4B400000u;
+constexpr float kMagicRound = 8388608.0f;   // 2^23: 0x4B000000 + n for n in [0, 2^23)
+constexpr uint32_t kMagicRoundBits = 0x4B000000u;
 constexpr double kScale40 = 1099511627776.0;    // generic path: masses in units of 2^-40
 constexpr double kInv40 = 1.0 / 1099511627776.0;
 
@@ -771,17 +777,36 @@ __global__ void __launch_bounds__(kSThreads, 5) topp_slice_kernel(StatsLaunch L)
   const float Gsf = live ? floorf(ms * c8) : 0.0f;
   const float bottom = Gsf - static_cast<float>(kNB - 1);
   unsigned* wh = sh.wh[warp];
-  // Plain (reorderable) exp2 and widening here, so the per-logit chains of
-  // different logits interleave around the shared-memory reductions.
-  auto add = [&](float x) {
-    const float fy = fmaxf(floorf(x * c8), bottom);
-    // l*c - (f+1)/8 (in [-1/8, 0] inside the window): the mass relative to
-    // the bin's upper edge.
-    const float t = fmaf(x, c, fmaf(fy, -0.125f, -0.125f));
-    const unsigned v = __float2uint_rn(ex2(t) * SliceShape<E>::kFix);
-    if (v) atomicAdd(&wh[static_cast<int>(Gsf - fy)], v);
-  };
-  if (live) {
+  if (live && fabsf(Gsf) < 4.0e6f) {
+    // |floor(l * c8)| < 2^22 across the window: the floor and the rounding to
+    // an integer by magic additions in the FP32 pipe (no conversion
+    // instruction); fy = max(floor(l * c8), bottom) and the bin Gs - fy come
+    // out of the mantissa bits.
+    const uint32_t whs = static_cast<uint32_t>(__cvta_generic_to_shared(wh));
+    const float gm = Gsf + kMagicFloor;
+    auto add = [&](float x) {
+      const float fy = fmaxf(__fadd_rd(x * c8, kMagicFloor) - kMagicFloor, bottom);
+      // l*c - (f+1)/8 (in [-1/8, 0] inside the window): the mass relative to
+      // the bin's upper edge.
+      const float t = fmaf(x, c, fmaf(fy, -0.125f, -0.125f));
+      const uint32_t v = __float_as_uint(fmaf(ex2(t), SliceShape<E>::kFix, kMagicRound)) - kMagicRoundBits;
+      const uint32_t idx = __float_as_uint(gm - fy) - kMagicFloorBits;
+      asm volatile("red.shared.add.u32 [%0], %1;" ::"r"(whs + idx * 4u), "r"(v) : "memory");
+    };
+#pragma unroll
+    for (int k = 0; k < VPT; ++k)
+#pragma unroll
+      for (int i = 0; i < EPV; ++i) add(Elem<E>::at(raw[k], i));
+    if (xv > -CUDART_INF_F) add(xv);
+  } else if (live) {
+    // Logits too large for the magic additions: the same bins by floorf and
+    // conversions.
+    auto add = [&](float x) {
+      const float fy = fmaxf(floorf(x * c8), bottom);
+      const float t = fmaf(x, c, fmaf(fy, -0.125f, -0.125f));
+      const unsigned v = __float2uint_rn(ex2(t) * SliceShape<E>::kFix);
+      if (v) atomicAdd(&wh[static_cast<int>(Gsf - fy)], v);
+    };
 #pragma unroll
     for (int k = 0; k < VPT; ++k)
 #pragma unroll

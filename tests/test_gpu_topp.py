@@ -111,3 +111,20 @@ def test_unaligned_rows(sv):
         rows = g.normal(0, 2, (5, V)).astype(np.float32)
         _check(sv, rows, "f32", 0.9, 0.9)
         _check(sv, rows, "bf16", 0.9, 0.9)
+
+
+@pytest.mark.parametrize("shift,T", [(4.0e5, 1.0), (-4.0e5, 1.0), (2.0e4, 0.01), (3.0e5, 0.5)])
+def test_large_logits_take_the_conversion_path(sv, shift, T):
+    """Logits so large that 8 * l * log2(e) / T leaves the range where the
+    bins are computed by magic-number additions (|floor| >= 4e6): those
+    slices are binned by floorf and conversions.  Rows mix such slices with
+    ordinary ones, and the values keep a spread of a few units (exactly
+    representable in fp32 at this magnitude), so the cut still falls among
+    many logits."""
+    g = np.random.default_rng(int(abs(shift)) + 7)
+    V = 40000
+    rows = np.round(g.normal(0, 2, (4, V)) * 64) / 64
+    rows = (rows + shift).astype(np.float32)
+    rows[1, : V // 2] = np.round(g.normal(0, 2, V // 2) * 64) / 64   # ordinary slices in the same row
+    rows[3] = np.round(rows[3])                                        # ties
+    _check(sv, rows, "f32", T, 0.9)
