@@ -70,6 +70,13 @@ struct RowDist {
   }
 };
 
+// p(x) of one id in double: exp2(l * c - mc) / K over the kept ids.
+__device__ __forceinline__ double exact_prob(const RowDist& d, float l, int j, float c, double K) {
+  if (d.tau != 0u && !kept(order_key(l), j, d.tau, d.cut)) return 0.0;
+  if (!(K > 0.0) || !(l > -CUDART_INF_F)) return 0.0;
+  return exp2(static_cast<double>(l) * static_cast<double>(c) - static_cast<double>(d.mc)) / K;
+}
+
 template <typename E>
 struct NodeRows {
   const E* lt;
@@ -84,6 +91,7 @@ struct TSShared {
   int depth[SV_MAX_TREE_NODES];
   double chunk_sum[kTSMaxChunks];
   double red[32];
+  double pq[2];
   RowDist pd[2];
   double bcast_d;
   int bcast_i;
@@ -92,17 +100,33 @@ struct TSShared {
   uint32_t status;
 };
 
-// max(0, p - cj q) of id j.
+// The coefficient c_j of the residual as an unevaluated sum of two floats,
+// hi + lo == c_j to about 2^-48 relative, so that p - c_j q keeps the
+// precision of p and q where they nearly cancel.
+struct Coef {
+  float hi, lo;
+};
+__device__ __forceinline__ Coef split_coef(double c) {
+  Coef k;
+  k.hi = static_cast<float>(c);
+  k.lo = static_cast<float>(c - static_cast<double>(k.hi));
+  return k;
+}
+
+// max(0, p - cj q) of id j: two fused multiply-adds with cj = hi + lo.
 template <typename E, bool FILTERED = true>
-__device__ __forceinline__ float resid(const NodeRows<E>& R, float lt, float ld, int j, float c, float cj) {
-  return fmaxf(0.0f, R.p.template at<FILTERED>(lt, j, c) - cj * R.q.template at<FILTERED>(ld, j, c));
+__device__ __forceinline__ float resid(const NodeRows<E>& R, float lt, float ld, int j, float c, Coef cj) {
+  const float q = R.q.template at<FILTERED>(ld, j, c);
+  return fmaxf(0.0f, fmaf(-cj.lo, q, fmaf(-cj.hi, q, R.p.template at<FILTERED>(lt, j, c))));
 }
 
 // Sum of max(0, p - cj q) over [j0, j1) by one warp: 16-byte loads with four
 // vectors of each row in flight per lane when both rows are aligned; the
-// draft row is not read when cj == 0 (the weights are p).
+// draft row is not read when cj == 0 (the weights are p).  Each lane sums in
+// fp32 (at most a chunk's share of the ids); the caller adds the lanes in
+// double.
 template <typename E, bool FILTERED, bool PONLY>
-__device__ __forceinline__ float chunk_residual(const NodeRows<E>& R, int j0, int j1, float c, float cj) {
+__device__ __forceinline__ float chunk_residual(const NodeRows<E>& R, int j0, int j1, float c, Coef cj) {
   constexpr int EPV = Elem<E>::kPerVec;
   constexpr int U = 4;
   const int lane = threadIdx.x & 31;
@@ -147,13 +171,13 @@ __device__ __forceinline__ float chunk_residual(const NodeRows<E>& R, int j0, in
 // chunk k (one warp per chunk, fp32 per lane, double across lanes); returns
 // the row total (double, the same in every thread).
 template <typename E>
-__device__ double residual_pass(const NodeRows<E>& R, const TreeSampleParams& P, float cj, TSShared& sh) {
+__device__ double residual_pass(const NodeRows<E>& R, const TreeSampleParams& P, Coef cj, TSShared& sh) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool filtered = (R.p.tau | R.q.tau) != 0u;
   for (int k = warp; k < P.nchunks; k += kTSWarps) {
     const int j0 = k * P.chunk, j1 = min(P.V, j0 + P.chunk);
     float s;
-    if (cj == 0.0f)
+    if (cj.hi == 0.0f)
       s = filtered ? chunk_residual<E, true, true>(R, j0, j1, P.c, cj) : chunk_residual<E, false, true>(R, j0, j1, P.c, cj);
     else
       s = filtered ? chunk_residual<E, true, false>(R, j0, j1, P.c, cj)
@@ -177,7 +201,7 @@ __device__ double residual_pass(const NodeRows<E>& R, const TreeSampleParams& P,
 // if rounding leaves u * total at or above the last prefix, the last id of
 // positive weight.
 template <typename E>
-__device__ int draw(const NodeRows<E>& R, const TreeSampleParams& P, float cj, double total, float u,
+__device__ int draw(const NodeRows<E>& R, const TreeSampleParams& P, Coef cj, double total, float u,
                     TSShared& sh) {
   const double target = static_cast<double>(u) * total;
   if (threadIdx.x < 32) {
@@ -325,10 +349,16 @@ __global__ void __launch_bounds__(kTSThreads) tree_sample_kernel(TreeSampleParam
     bool sums_for_cj = false;  // chunk sums of the current residual are in shared memory
     int next = -1;
     for (int ch = sh.first_child[node]; ch >= 0; ch = sh.next_sib[ch]) {
-      if (threadIdx.x == 0) {
+      // The accept test in double: p(x) (thread 0) and q(x) (thread 1) from
+      // the rows' offsets and kept masses with the double-precision exp2.
+      if (threadIdx.x < 2) {
         const int x = tok[ch];
-        const double p = R.p.at(Elem<E>::load(R.lt + x), x, P.c);
-        const double q = R.q.at(Elem<E>::load(R.ld + x), x, P.c);
+        sh.pq[threadIdx.x] = threadIdx.x == 0 ? exact_prob(R.p, Elem<E>::load(R.lt + x), x, P.c, P.ts[row].K)
+                                              : exact_prob(R.q, Elem<E>::load(R.ld + x), x, P.c, P.ds[row].K);
+      }
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        const double p = sh.pq[0], q = sh.pq[1];
         const double u = P.u_accept[base + ch];
         sh.bcast_i = u * q * W < fmax(0.0, p - cj * q);
       }
@@ -340,7 +370,7 @@ __global__ void __launch_bounds__(kTSThreads) tree_sample_kernel(TreeSampleParam
         break;
       }
       const double c_new = cj + W;
-      const double W_new = residual_pass(R, P, static_cast<float>(c_new), sh);
+      const double W_new = residual_pass(R, P, split_coef(c_new), sh);
       if (W_new > 0.0) {
         cj = c_new;
         W = W_new;
@@ -359,8 +389,8 @@ __global__ void __launch_bounds__(kTSThreads) tree_sample_kernel(TreeSampleParam
       }
       continue;
     }
-    double total = sums_for_cj ? W : residual_pass(R, P, static_cast<float>(cj), sh);
-    const int y = draw(R, P, static_cast<float>(cj), total, P.u_final[b], sh);
+    double total = sums_for_cj ? W : residual_pass(R, P, split_coef(cj), sh);
+    const int y = draw(R, P, split_coef(cj), total, P.u_final[b], sh);
     if (threadIdx.x == 0) {
       out[d] = y;
       P.accept_len[b] = d;

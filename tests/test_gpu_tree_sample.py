@@ -6,11 +6,12 @@ the zero-residual fallback, and invalid trees.
 
 The path, accept length and every emitted token must equal the oracle's.
 A tree may differ only where one of the oracle's decisions on it lies
-within NEAR of its threshold (in units of the uniform): the GPU forms p and
-q in fp32 (exp2 of the scaled logit, times 1/K) and sums the residual mass
-max(0, p - c q) in fp32 per lane and fp64 across lanes, about 1e-6 relative
-on the mass, which the accept test r(x)/q(x) divides by.  Such trees are
-counted, and must stay rare.
+within NEAR = 1e-6 of its threshold (in units of the uniform), the same
+margin as the chain verify.  The GPU takes each accept test in double (p(x)
+and q(x) with the double-precision exp2), forms the residual max(0, p - c q)
+per id with c split into two floats (so p - c q keeps the precision of p and
+q where they nearly cancel), and sums it in fp32 per lane of a chunk and in
+fp64 across lanes.  Such trees are counted, and must stay rare.
 """
 import numpy as np
 import pytest
@@ -22,7 +23,7 @@ from _parity import logits_tensor, t
 
 pytestmark = pytest.mark.gpu
 
-NEAR = 1e-5
+NEAR = O.NEAR  # 1e-6
 
 
 @pytest.fixture(scope="module")
@@ -97,7 +98,7 @@ def test_many_siblings_tiny_vocab(sv, N, V, D, dtype, noise):
     tr = synth.make_tree_sample_inputs(cfg, seed=N + V, draft_noise=noise)
     got = _run(sv, tr, 1.0, 1.0, dtype)
     want = _oracle(tr, 1.0, 1.0)
-    _compare(got, want, max_near_frac=0.34)
+    _compare(got, want)
 
 
 def test_unaligned_rows_and_large_vocab(sv):
