@@ -8,7 +8,12 @@ from __future__ import annotations
 import ctypes
 import os
 
-LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libspec_verify.so")
+_HERE = os.path.dirname(os.path.abspath(__file__))
+# SPEC_VERIFY_LIBRARY selects another build of the same C-ABI, e.g. the
+# bounds-checked debug build libspec_verify_debug.so (its index checks
+# report through sv_debug_flags).
+LIB_PATH = os.environ.get("SPEC_VERIFY_LIBRARY") or os.path.join(_HERE, "libspec_verify.so")
+DEBUG_LIB_PATH = os.path.join(_HERE, "libspec_verify_debug.so")
 
 SV_OK = 0
 SV_ERR_INVALID_ARGUMENT = 1
@@ -30,6 +35,8 @@ SV_MAX_GAMMA = 64
 SV_MAX_VOCAB = 16777216
 SV_MAX_TREE_NODES = 1024
 SV_MAX_TREE_DEPTH = 64
+
+SV_DEBUG_INDEX = 1
 
 
 class ChainDesc(ctypes.Structure):
@@ -94,6 +101,7 @@ SIGNATURES = {
     "sv_version": (_I32, []),
     "sv_set_phase_events": (None, [_P, _I32]),
     "sv_launch_count": (ctypes.c_uint64, []),
+    "sv_debug_flags": (ctypes.c_uint32, [_I32]),
 }
 
 _lib = None

@@ -343,7 +343,29 @@ void end_call() {
 }
 }  // namespace sv
 
+namespace {
+constexpr int kMaxDebugReaders = 32;
+sv::DebugReader g_debug_readers[kMaxDebugReaders];
+std::atomic<int> g_debug_nreaders{0};
+}  // namespace
+
+namespace sv {
+int register_debug_reader(DebugReader r) {
+  const int i = g_debug_nreaders.fetch_add(1);
+  if (i < kMaxDebugReaders) g_debug_readers[i] = r;
+  return i;
+}
+unsigned read_debug_words(bool reset) {
+  unsigned v = 0;
+  const int n = g_debug_nreaders.load();
+  for (int i = 0; i < n && i < kMaxDebugReaders; ++i) v |= g_debug_readers[i](reset);
+  return v;
+}
+}  // namespace sv
+
 extern "C" {
+uint32_t sv_debug_flags(int32_t reset) { return sv::read_debug_words(reset != 0); }
+
 void sv_set_phase_events(void* const* events, int32_t n) {
   if (!events || n <= 0) {
     sv::end_call();

@@ -105,7 +105,7 @@ __global__ void __launch_bounds__(THREADS) stats_stream_kernel(StatsLaunch L) {
     if (!(M > -CUDART_INF_F)) st.status |= SV_ROW_EMPTY;
     const Query q = row_query(S, r);
     if (q.bad) st.status |= SV_ROW_BAD_DRAFT_ID;
-    if (q.elem >= 0 && !(st.status & SV_ROW_EMPTY))
+    if (q.elem >= 0 && !(st.status & SV_ROW_EMPTY) && sv_in(q.elem, S.len))
       st.e_query = weight(Elem<E>::load(row + q.elem), c, st.mc);
     S.out[r] = st;
   }

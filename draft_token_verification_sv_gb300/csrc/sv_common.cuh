@@ -12,6 +12,23 @@ namespace sv {
 
 namespace cg = cooperative_groups;
 
+// Debug builds (-DSV_DEBUG): index checks on computed and data-dependent
+// accesses.  A failed check sets a bit in this translation unit's debug word
+// (read through sv_debug_flags) and the caller skips the access; nothing
+// traps.  Release builds compile the checks away.
+constexpr unsigned kDebugIndex = 1u;  // an index outside its buffer
+#ifdef SV_DEBUG
+static __device__ unsigned int g_sv_debug_word;
+__device__ __forceinline__ bool sv_check(bool ok, unsigned bit) {
+  if (!ok) atomicOr(&g_sv_debug_word, bit);
+  return ok;
+}
+#else
+__device__ __forceinline__ constexpr bool sv_check(bool, unsigned) { return true; }
+#endif
+// 0 <= i < n, checked in debug builds.
+__device__ __forceinline__ bool sv_in(long long i, long long n) { return sv_check(i >= 0 && i < n, kDebugIndex); }
+
 // Masses of the top-p search are summed exactly as integers: each
 // exp((l - m)/T) in (0, 1] is rounded to a multiple of 2^-40.  With at most
 // 2^24 elements the sums stay below 2^64 and the result does not depend on

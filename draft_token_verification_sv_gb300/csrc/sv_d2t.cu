@@ -72,7 +72,7 @@ scatter_fill_kernel(const E* __restrict__ in, int64_t in_stride, const int32_t* 
   __syncthreads();
   for (int j = threadIdx.x; j < vd; j += THREADS) {
     const int x = __ldg(d2t + j);
-    if (x >= 0 && x < V) dst[x] = src[j];
+    if (x >= 0 && sv_in(x, V)) dst[x] = src[j];
   }
 }
 

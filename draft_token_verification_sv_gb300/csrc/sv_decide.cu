@@ -122,7 +122,7 @@ __device__ __forceinline__ void chunk_weights(const DecideParams& P, const RowVi
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
       const int jd = j0 + e < P.V ? __ldg(P.t2d + j0 + e) : -1;
-      ld[e] = (jd >= 0 && jd < P.Vd) ? Elem<ED>::load(drow + jd) : -CUDART_INF_F;
+      ld[e] = (jd >= 0 && sv_in(jd, P.Vd)) ? Elem<ED>::load(drow + jd) : -CUDART_INF_F;
     }
   }
 #pragma unroll
@@ -163,7 +163,7 @@ __device__ __forceinline__ void segment_sums_fast(const DecideParams& P, const R
         for (int e = 0; e < 8; ++e) {
           const int4& v = m[q][e >> 2];
           const int jd = (e & 3) == 0 ? v.x : (e & 3) == 1 ? v.y : (e & 3) == 2 ? v.z : v.w;
-          ld[q][e] = (jd >= 0 && jd < P.Vd) ? Elem<ED>::load(drow + jd) : -CUDART_INF_F;
+          ld[q][e] = (jd >= 0 && sv_in(jd, P.Vd)) ? Elem<ED>::load(drow + jd) : -CUDART_INF_F;
         }
       }
     } else {
@@ -371,7 +371,7 @@ __global__ void __launch_bounds__(kDThreads, NC >= 8 ? 2 : 4) decide_kernel(Deci
     for (int sg = tid; sg < nseg; sg += kDThreads) slast[sg] = sg == 0 ? lpf : -1;
     __syncthreads();
   }
-  if (sh.total > 0.0 && sh.chunk >= 0) {
+  if (sh.total > 0.0 && sh.chunk >= 0 && sv_in(sh.chunk, nchunks)) {
     // Rescan the chunk that holds the draw: the thread whose ids span
     // u * total (in block order) finds the id.
     const int j0 = sh.chunk * kDChunk + tid * kDEPT;
@@ -401,7 +401,7 @@ __global__ void __launch_bounds__(kDThreads, NC >= 8 ? 2 : 4) decide_kernel(Deci
     if (tid == 0 && sh.best != INT32_MAX) sh.tok = sh.best;
     __syncthreads();
   }
-  const int tok = sh.tok;
+  const int tok = sv_in(sh.tok, V) ? sh.tok : -1;
   for (int i = tid; i <= G; i += kDThreads)
     out[i] = i < k ? P.ids[static_cast<int64_t>(b) * G + i] : (i == k ? tok : -1);
   if (tid == 0) {

@@ -199,7 +199,7 @@ __device__ void tree_walk(const GreedyParams& P, int b) {
     for (int n = threadIdx.x; n < N; n += THREADS)
       if (s_depth[n] == lvl) {
         const int par = s_par[n];
-        s_acc[n] = (s_acc[par] && s_tok[n] == s_g[par]) ? 1 : 0;
+        s_acc[n] = (sv_in(par, N) && s_acc[par] && s_tok[n] == s_g[par]) ? 1 : 0;
       }
   }
   __syncthreads();
@@ -213,9 +213,10 @@ __device__ void tree_walk(const GreedyParams& P, int b) {
   key = block_max_u64<THREADS>(key, s_red);
   const int best = static_cast<int>(0xffffffffu - static_cast<uint32_t>(key & 0xffffffffull));
   const int L = static_cast<int>(key >> 32);
-  if (threadIdx.x == 0) {
+  if (threadIdx.x == 0 && sv_in(best, N) && sv_in(L, D + 1)) {
     int cur = best;
     for (int d = L; d >= 0; --d) {  // L <= D steps
+      if (!sv_in(cur, N)) break;
       path[d] = cur;
       if (d > 0) out[d - 1] = s_tok[cur];
       if (d > 0) cur = s_par[cur];

@@ -9,6 +9,12 @@ namespace sv {
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Debug builds: every translation unit registers a reader of its debug
+// word (returns it; clears it when asked).  sv_debug_flags ORs them.
+using DebugReader = unsigned (*)(bool reset);
+int register_debug_reader(DebugReader r);
+unsigned read_debug_words(bool reset);
+
 // Call once before the first device operation of a public call: records
 // the caller's first phase event, if one is pending (sv_set_phase_events).
 void start_phases(cudaStream_t stream);
@@ -136,5 +142,20 @@ sv_status d2t_scatter(const void* in, int64_t in_stride, const int32_t* d2t, con
                       int64_t out_stride, cudaStream_t stream);
 sv_status build_t2d(const int32_t* d2t, int vd, int v, int32_t* t2d, int32_t* status,
                     cudaStream_t stream);
+
+#ifdef SV_DEBUG
+// This translation unit's debug word reader, registered at load time.
+static unsigned read_this_debug_word(bool reset) {
+  unsigned v = 0;
+  if (cudaDeviceSynchronize() != cudaSuccess) return ~0u;
+  if (cudaMemcpyFromSymbol(&v, g_sv_debug_word, sizeof(v)) != cudaSuccess) return ~0u;
+  if (reset) {
+    const unsigned z = 0;
+    if (cudaMemcpyToSymbol(g_sv_debug_word, &z, sizeof(z)) != cudaSuccess) return ~0u;
+  }
+  return v;
+}
+[[maybe_unused]] static const int g_debug_reader_registered = register_debug_reader(&read_this_debug_word);
+#endif
 
 }  // namespace sv

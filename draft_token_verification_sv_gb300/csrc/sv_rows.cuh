@@ -95,7 +95,7 @@ __device__ __forceinline__ Query row_query(const RowSet& S, int r) {
     return q;
   }
   q.sec = x;
-  q.elem = S.t2d ? S.t2d[x] : x;
+  q.elem = S.t2d ? (sv_in(x, S.vocab) ? S.t2d[x] : -1) : x;
   if (q.elem >= S.len) q.elem = -1;  // a t2d entry outside the draft row maps nowhere
   return q;
 }

@@ -196,7 +196,8 @@ __global__ void __launch_bounds__(kKThreads, 2) topk_kernel(const E* __restrict_
       int rank = 0;
       for (int j = 0; j < n; ++j) rank += s_key[j] > mine;
       if (rank < k) {
-        oi[rank] = argmax_index(mine);
+        const int id = argmax_index(mine);
+        oi[rank] = sv_in(id, V) ? id : -1;
         if (ov) ov[rank] = value_of_key(static_cast<uint32_t>(mine >> 32));
       }
     } else if (static_cast<int>(threadIdx.x) < k) {  // fewer than k logits that are not NaN

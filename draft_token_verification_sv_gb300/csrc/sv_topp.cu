@@ -995,7 +995,10 @@ __global__ void __launch_bounds__(kSThreads, 5) topp_slice_kernel(StatsLaunch L)
       generic = n == 0 || n > kCandCap;
       if (!generic) {
         // The candidates' logits: one parallel round of loads (served by L2).
-        for (int i = tid; i < n; i += kSThreads) sh.cand.x[i] = load_at<E>(row, sh.cand.j[i]);
+        for (int i = tid; i < n; i += kSThreads) {
+          const int j = sh.cand.j[i];
+          sh.cand.x[i] = sv_in(j, S.len) ? load_at<E>(row, j) : -CUDART_INF_F;
+        }
         __syncthreads();
       }
       if (!generic)
@@ -1017,7 +1020,7 @@ __global__ void __launch_bounds__(kSThreads, 5) topp_slice_kernel(StatsLaunch L)
     st.e_query = 0.0f;
     const Query q = row_query(S, r);
     if (q.bad) st.status |= SV_ROW_BAD_DRAFT_ID;
-    if (q.elem >= 0 && !empty) {
+    if (q.elem >= 0 && !empty && sv_in(q.elem, S.len)) {
       const float x = Elem<E>::load(row + q.elem);
       if (kept(order_key(x), q.sec, tau, cut)) st.e_query = weight(x, c, mc);
     }

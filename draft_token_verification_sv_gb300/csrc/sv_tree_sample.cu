@@ -353,8 +353,11 @@ __global__ void __launch_bounds__(kTSThreads) tree_sample_kernel(TreeSampleParam
       // the rows' offsets and kept masses with the double-precision exp2.
       if (threadIdx.x < 2) {
         const int x = tok[ch];
-        sh.pq[threadIdx.x] = threadIdx.x == 0 ? exact_prob(R.p, Elem<E>::load(R.lt + x), x, P.c, P.ts[row].K)
-                                              : exact_prob(R.q, Elem<E>::load(R.ld + x), x, P.c, P.ds[row].K);
+        double v = 0.0;
+        if (sv_in(x, P.V))
+          v = threadIdx.x == 0 ? exact_prob(R.p, Elem<E>::load(R.lt + x), x, P.c, P.ts[row].K)
+                               : exact_prob(R.q, Elem<E>::load(R.ld + x), x, P.c, P.ds[row].K);
+        sh.pq[threadIdx.x] = v;
       }
       __syncthreads();
       if (threadIdx.x == 0) {
@@ -383,7 +386,7 @@ __global__ void __launch_bounds__(kTSThreads) tree_sample_kernel(TreeSampleParam
     if (next >= 0) {
       node = next;
       ++d;
-      if (threadIdx.x == 0) {
+      if (threadIdx.x == 0 && sv_in(d, L)) {
         path[d] = node;
         out[d - 1] = tok[node];
       }

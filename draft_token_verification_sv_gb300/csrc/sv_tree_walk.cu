@@ -216,7 +216,7 @@ __global__ void __launch_bounds__(kWThreads) walk_level_kernel(WalkParams P, int
   if (level < P.D) {
     for (int c = 1 + threadIdx.x; c < N; c += kWThreads) {
       const int p = par[c];
-      if (s_g[p] >= 0 && tok[c] == s_g[p]) {
+      if (sv_in(p, N) && s_g[p] >= 0 && tok[c] == s_g[p]) {
         const int slot = atomicAdd(&s_next_n, 1);
         P.frontier[tb + slot] = c;  // the frontier was copied to shared memory
       }
@@ -240,6 +240,7 @@ __global__ void __launch_bounds__(kWThreads) walk_level_kernel(WalkParams P, int
       int32_t* out = P.out_tokens + static_cast<int64_t>(b) * L;
       int cur = best;
       for (int d = level; d >= 0; --d) {
+        if (!sv_in(cur, N) || !sv_in(d, L)) break;
         path[d] = cur;
         if (d > 0) out[d - 1] = tok[cur];
         if (d > 0) cur = par[cur];

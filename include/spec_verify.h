@@ -394,6 +394,20 @@ sv_status sv_softmax_topp(const sv_sample_desc* desc, const void* logits, float*
 void sv_set_phase_events(void* const* events, int32_t n);
 uint64_t sv_launch_count(void);
 
+/*
+ * Bounds-check flags of the debug build (the same sources compiled with
+ * -DSV_DEBUG, as libspec_verify_debug.so).  There, every computed or
+ * data-dependent index into a caller buffer or a table (a t2d or d2t entry,
+ * a parent id, a query element, a draw's chunk or token, a tree walk) is
+ * checked before the access; a failed check skips the access and sets bit
+ * SV_DEBUG_INDEX in a device word.  No check traps.  sv_debug_flags waits
+ * for the device (cudaDeviceSynchronize), returns the OR of the words and
+ * clears them when reset != 0.  ~0u: the words could not be read (a CUDA
+ * error).  The release build checks nothing and returns 0.
+ */
+#define SV_DEBUG_INDEX 1u
+uint32_t sv_debug_flags(int32_t reset);
+
 /* Static description of a status code. */
 const char* sv_status_string(sv_status status);
 
