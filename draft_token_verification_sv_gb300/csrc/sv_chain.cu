@@ -239,6 +239,7 @@ sv_status sampling_chain(const ChainArgs& a, cudaStream_t stream) {
   P.ids = a.ids;
   P.u_resample = a.u_resample;
   P.t2d = a.d2t ? a.t2d : nullptr;
+  P.d2t = a.d2t ? a.d2t : nullptr;
   P.out_tokens = a.out_tokens;
   P.num_accepted = a.num_accepted;
   P.row_status = a.row_status;

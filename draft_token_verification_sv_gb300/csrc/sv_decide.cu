@@ -20,6 +20,15 @@
 // per row) scans the chunk sums, finds the chunk that holds u * total and
 // rescans that one chunk (from L2) with a block-wide prefix scan to pick the
 // token.
+//
+// EAGLE3 draft rows (a d2t map; "SSD: extending the engine with new models
+// and an EAGLE3 draft" §六): when d2t is strictly increasing, the draft ids
+// whose target ids fall in a block's segment form one contiguous range
+// (tabulated per call by d2t_range_kernel), so the block reads that range of
+// the draft row and of d2t with plain coalesced loads and applies
+// max(0, p - q) in shared memory, instead of a t2d lookup and a dependent
+// gather per target id.  Per-id weights and the order of every sum are those
+// of the t2d path, which stays in use for any other d2t.
 #include "sv_rows.cuh"
 
 namespace sv {
@@ -38,6 +47,8 @@ struct DecideShared {
   int red_i[32];
   int k;
   unsigned status;
+  int a0, a1;     // this segment's draft-id range (draft-range table)
+  unsigned bad;   // entries of d2t that break the table
   int last;
   int chunk;
   int tok;
@@ -131,62 +142,164 @@ __device__ __forceinline__ void chunk_weights(const DecideParams& P, const RowVi
 }
 
 // Per-thread draw-weight sums of the NC chunks c0.. of this block with every
-// load of the segment in flight together (R.fast only); groups of 8 ids past
-// the row add nothing.  lp: the largest id with a positive weight.
-template <typename ET, typename ED, int NC>
+// load of the segment in flight together (R.fast, draft rows without t2d
+// only); groups of 8 ids past the row add nothing.  lp: the largest id with
+// a positive weight.
+template <typename ET, typename ED, int NC, bool MAY_RESID = true>
 __device__ __forceinline__ void segment_sums_fast(const DecideParams& P, const RowView& R, int c0, bool resid,
                                                   const DrawSide& pt, const DrawSide& pd, float* part, int& lp) {
   const ET* trow = static_cast<const ET*>(R.trow);
   const ED* drow = static_cast<const ED*>(R.drow);
   const int tj = static_cast<int>(threadIdx.x) * kDEPT;
-  Raw8<ET> rt[NC];
-  bool ok[NC];
+  // Chunks in flight together: all of them, or two at a time for fp32 target
+  // rows, whose raw vectors with the draft's would not fit the registers.
+  constexpr int kGrp = (sizeof(ET) == 4 && NC > 2) ? 2 : NC;
 #pragma unroll
-  for (int q = 0; q < NC; ++q) {
-    const int j0 = (c0 + q) * kDChunk + tj;
-    ok[q] = j0 < P.V;  // V is a multiple of 8: a group is wholly in or out
-    raw_load(rt[q], trow + (ok[q] ? j0 : 0));
-  }
-  float ld[NC][8];
-  if (resid) {
-    if (P.t2d) {
-      int4 m[NC][2];
+  for (int g0 = 0; g0 < NC; g0 += kGrp) {
+    Raw8<ET> rt[kGrp];
+    bool ok[kGrp];
 #pragma unroll
-      for (int q = 0; q < NC; ++q) {
-        const int4* src = reinterpret_cast<const int4*>(P.t2d + (ok[q] ? (c0 + q) * kDChunk + tj : 0));
-        m[q][0] = __ldg(src);
-        m[q][1] = __ldg(src + 1);
-      }
+    for (int q = 0; q < kGrp; ++q) {
+      const int j0 = (c0 + g0 + q) * kDChunk + tj;
+      ok[q] = j0 < P.V;  // V is a multiple of 8: a group is wholly in or out
+      raw_load(rt[q], trow + (ok[q] ? j0 : 0));
+    }
+    float ld[kGrp][8];
+    if (MAY_RESID && resid) {
+      Raw8<ED> rd[kGrp];
 #pragma unroll
-      for (int q = 0; q < NC; ++q) {
+      for (int q = 0; q < kGrp; ++q) raw_load(rd[q], drow + (ok[q] ? (c0 + g0 + q) * kDChunk + tj : 0));
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int4& v = m[q][e >> 2];
-          const int jd = (e & 3) == 0 ? v.x : (e & 3) == 1 ? v.y : (e & 3) == 2 ? v.z : v.w;
-          ld[q][e] = (jd >= 0 && sv_in(jd, P.Vd)) ? Elem<ED>::load(drow + jd) : -CUDART_INF_F;
-        }
-      }
-    } else {
-      Raw8<ED> rd[NC];
-#pragma unroll
-      for (int q = 0; q < NC; ++q) raw_load(rd[q], drow + (ok[q] ? (c0 + q) * kDChunk + tj : 0));
-#pragma unroll
-      for (int q = 0; q < NC; ++q) {
+      for (int q = 0; q < kGrp; ++q) {
 #pragma unroll
         for (int e = 0; e < 8; ++e) ld[q][e] = raw_at(rd[q], e);
       }
     }
+#pragma unroll
+    for (int q = 0; q < kGrp; ++q) {
+      const int j0 = (c0 + g0 + q) * kDChunk + tj;
+      float s = 0.0f;
+      if (ok[q]) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float w =
+              draw_weight(raw_at(rt[q], e), resid ? ld[q][e] : -CUDART_INF_F, j0 + e, resid, P.c, pt, pd);
+          s += w;
+          if (w > 0.0f) lp = j0 + e;
+        }
+      }
+      part[g0 + q] = s;
+    }
   }
+}
+
+// Residual draw weights of this block's segment through the draft-range
+// table: p(j) of the target segment into wbuf (shared memory), then for every
+// draft id jd whose target id x = d2t[jd] lies in the segment (the ids
+// [d2t_first[seg], d2t_first[seg + 1])) wbuf[x] = max(0, p(x) - q(jd)); ids
+// without a draft entry keep p(x) = max(0, p(x) - 0).  Per-thread sums then
+// run over the thread's own ids in id order, as in segment_sums_fast.
+// 16-byte asynchronous copy global -> shared (L2 only), and the wait for all
+// of this thread's copies.
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  const uint32_t sa = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+template <typename ET, typename ED, int NC>
+__device__ __forceinline__ void segment_sums_compact(const DecideParams& P, const RowView& R, int a0, int a1,
+                                                     int c0, const DrawSide& pt, const DrawSide& pd, float* wbuf,
+                                                     float* part, int& lp) {
+  const ET* trow = static_cast<const ET*>(R.trow);
+  const ED* drow = static_cast<const ED*>(R.drow);
+  const int tid = static_cast<int>(threadIdx.x);
+  const int tj = tid * kDEPT;
+  const int s0 = c0 * kDChunk;
+  bool ok[NC];
+#pragma unroll
+  for (int q = 0; q < NC; ++q) ok[q] = (c0 + q) * kDChunk + tj < P.V;  // V is a multiple of 8
+  // fp32 targets land in wbuf by asynchronous copies (no registers held while
+  // in flight) and are turned into p(j) in place; bf16 targets come through
+  // registers.
+  Raw8<ET> rt[sizeof(ET) == 2 ? NC : 1];
+  if constexpr (sizeof(ET) == 4) {
+#pragma unroll
+    for (int q = 0; q < NC; ++q) {
+      float* dst = wbuf + q * kDChunk + tj;
+      if (ok[q]) {
+        const ET* src = trow + (c0 + q) * kDChunk + tj;
+        cp_async16(dst, src);
+        cp_async16(dst + 4, src + 4);
+      }
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  } else {
+#pragma unroll
+    for (int q = 0; q < NC; ++q) raw_load(rt[q], trow + (ok[q] ? (c0 + q) * kDChunk + tj : 0));
+  }
+  // The first draft ids of the range, loaded while the target is in flight.
+  constexpr int kPre = 8;
+  int xd[kPre];
+  float ldv[kPre];
+#pragma unroll
+  for (int u = 0; u < kPre; ++u) {
+    const int jd = a0 + u * kDThreads + tid;
+    xd[u] = -1;
+    ldv[u] = -CUDART_INF_F;
+    if (jd < a1) {
+      xd[u] = __ldg(P.d2t + jd);
+      ldv[u] = Elem<ED>::load(drow + jd);
+    }
+  }
+  if constexpr (sizeof(ET) == 4) cp_async_wait_all();
+#pragma unroll
+  for (int q = 0; q < NC; ++q) {
+    const int j0 = (c0 + q) * kDChunk + tj;
+    float4* slot = reinterpret_cast<float4*>(wbuf + q * kDChunk + tj);
+    float x[8];
+    if constexpr (sizeof(ET) == 4) {
+      const float4 lo = ok[q] ? slot[0] : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      const float4 hi = ok[q] ? slot[1] : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      x[0] = lo.x; x[1] = lo.y; x[2] = lo.z; x[3] = lo.w;
+      x[4] = hi.x; x[5] = hi.y; x[6] = hi.z; x[7] = hi.w;
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) x[e] = raw_at(rt[q], e);
+    }
+    float w[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) w[e] = ok[q] ? fmaxf(0.0f, prob_of(x[e], j0 + e, P.c, pt)) : 0.0f;
+    slot[0] = make_float4(w[0], w[1], w[2], w[3]);
+    slot[1] = make_float4(w[4], w[5], w[6], w[7]);
+  }
+  __syncthreads();
+  constexpr int kSeg = NC * kDChunk;
+  auto apply = [&](int x, float ld) {
+    const int t = x - s0;
+    if (ld > -CUDART_INF_F && sv_in(t, kSeg)) {
+      const float qv = prob_of(ld, x, P.c, pd);
+      wbuf[t] = fmaxf(0.0f, wbuf[t] - qv);
+    }
+  };
+#pragma unroll
+  for (int u = 0; u < kPre; ++u)
+    if (xd[u] >= 0) apply(xd[u], ldv[u]);
+#pragma unroll 4
+  for (int jd = a0 + kPre * kDThreads + tid; jd < a1; jd += kDThreads) apply(__ldg(P.d2t + jd), Elem<ED>::load(drow + jd));
+  __syncthreads();
 #pragma unroll
   for (int q = 0; q < NC; ++q) {
     const int j0 = (c0 + q) * kDChunk + tj;
     float s = 0.0f;
     if (ok[q]) {
+      const float4* src = reinterpret_cast<const float4*>(wbuf + q * kDChunk + tj);
+      const float4 lo = src[0], hi = src[1];
+      const float w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        const float w = draw_weight(raw_at(rt[q], e), resid ? ld[q][e] : -CUDART_INF_F, j0 + e, resid, P.c, pt, pd);
-        s += w;
-        if (w > 0.0f) lp = j0 + e;
+        s += w[e];
+        if (w[e] > 0.0f) lp = j0 + e;
       }
     }
     part[q] = s;
@@ -206,14 +319,25 @@ __device__ __forceinline__ float block_sum_to0(float v, DecideShared& sh) {
   return s;
 }
 
-template <typename ET, typename ED, int NC>
-__global__ void __launch_bounds__(kDThreads, NC >= 8 ? 2 : 4) decide_kernel(DecideParams P, int nseg) {
+// COMPACT: the draft-range table is in use (d2t with t2d); the block then
+// holds NC * kDChunk floats of dynamic shared memory.
+template <typename ET, typename ED, int NC, bool COMPACT>
+__global__ void __launch_bounds__(kDThreads, COMPACT ? (NC >= 8 ? 3 : 5) : (NC >= 8 ? 2 : 4)) decide_kernel(DecideParams P, int nseg) {
   __shared__ DecideShared sh;
+  extern __shared__ __align__(16) float wbuf[];
   const int b = blockIdx.x / nseg;
   const int seg = blockIdx.x - b * nseg;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = P.G, V = P.V;
   const int nchunks = (V + kDChunk - 1) / kDChunk;
+
+  // This segment's draft range and the table's validity, fetched together
+  // with the record.
+  if constexpr (COMPACT) {
+    if (tid == 32) sh.a0 = __ldg(P.d2t_first + seg);
+    if (tid == 33) sh.a1 = __ldg(P.d2t_first + seg + 1);
+    if (tid == 34) sh.bad = __ldcg(P.counters + P.B);
+  }
 
   // The batch row's decisions: made by the statistics pass (one thread
   // fetches the record), or here by warp 0.
@@ -254,7 +378,15 @@ __global__ void __launch_bounds__(kDThreads, NC >= 8 ? 2 : 4) decide_kernel(Deci
   const int c0 = seg * NC;
   float part[NC];
   int lp = -1;
-  if (R.fast) {
+  // The draft-range table is usable when d2t is strictly increasing within
+  // [0, V) (no entry counted by d2t_range_kernel).
+  bool compact = false;
+  if constexpr (COMPACT) compact = resid && R.fast && sh.bad == 0u;
+  if (compact) {
+    segment_sums_compact<ET, ED, NC>(P, R, sh.a0, sh.a1, c0, pt, pd, wbuf, part, lp);
+  } else if (COMPACT && R.fast && !resid) {
+    segment_sums_fast<ET, ED, NC, false>(P, R, c0, false, pt, pd, part, lp);
+  } else if (!COMPACT && R.fast && !(resid && P.t2d)) {
     segment_sums_fast<ET, ED, NC>(P, R, c0, resid, pt, pd, part, lp);
   } else {
 #pragma unroll 1
@@ -416,26 +548,69 @@ __global__ void __launch_bounds__(kDThreads, NC >= 8 ? 2 : 4) decide_kernel(Deci
 }
 
 size_t decide_scratch_bytes(int B, int V) {
-  const size_t chunks = static_cast<size_t>(B) * static_cast<size_t>((V + kDChunk - 1) / kDChunk);
+  const size_t nchunks = static_cast<size_t>((V + kDChunk - 1) / kDChunk);
+  const size_t chunks = static_cast<size_t>(B) * nchunks;
   return align_up(chunks * sizeof(float), 256) + align_up(chunks * sizeof(int32_t), 256) +
-         align_up(static_cast<size_t>(B) * sizeof(unsigned), 256);
+         align_up((static_cast<size_t>(B) + 1) * sizeof(unsigned), 256) + align_up((nchunks + 2) * sizeof(int32_t), 256);
+}
+
+// The draft-range table of the draw: first[s] = the first draft id whose
+// target id is at least s * seg_ids, for s = 0..nseg (Vd when none).  It is
+// meaningful when d2t is strictly increasing with every entry in [0, V); each
+// entry that breaks this adds one to *bad (zero before the launch), and the
+// draw then uses t2d instead.  One thread per draft id (at least nseg + 1).
+__global__ void d2t_range_kernel(const int32_t* __restrict__ d2t, int Vd, int V, int seg_ids, int nseg,
+                                 int32_t* __restrict__ first, unsigned* bad) {
+  const int jd = static_cast<int>(blockIdx.x * blockDim.x + threadIdx.x);
+  if (Vd == 0) {
+    if (jd <= nseg) first[jd] = 0;
+    return;
+  }
+  if (jd >= Vd) return;
+  const int x = d2t[jd];
+  const int xp = jd > 0 ? d2t[jd - 1] : -1;
+  if (x < 0 || x >= V || x <= xp) {
+    atomicAdd(bad, 1u);
+    return;
+  }
+  const int cur = x / seg_ids;
+  const int prev = xp >= 0 ? xp / seg_ids : -1;
+  for (int s = prev + 1; s <= cur && s <= nseg; ++s) first[s] = jd;
+  if (jd == Vd - 1)
+    for (int s = cur + 1; s <= nseg; ++s) first[s] = Vd;
 }
 
 template <typename ET, typename ED, int NC>
 static sv_status launch_decide_typed(DecideParams P, void* scratch, cudaStream_t stream) {
+  static FuncAttrCache cache;
   const int nchunks = (P.V + kDChunk - 1) / kDChunk;
   const int nseg = (nchunks + NC - 1) / NC;
   const size_t chunks = static_cast<size_t>(P.B) * nchunks;
   char* s = static_cast<char*>(scratch);
+  const size_t o_last = align_up(chunks * sizeof(float), 256);
+  const size_t o_cnt = o_last + align_up(chunks * sizeof(int32_t), 256);
+  const size_t o_first = o_cnt + align_up((static_cast<size_t>(P.B) + 1) * sizeof(unsigned), 256);
   P.chunk_sums = reinterpret_cast<float*>(s);
-  P.seg_last = reinterpret_cast<int32_t*>(s + align_up(chunks * sizeof(float), 256));
-  P.counters = reinterpret_cast<unsigned*>(s + align_up(chunks * sizeof(float), 256) +
-                                           align_up(chunks * sizeof(int32_t), 256));
+  P.seg_last = reinterpret_cast<int32_t*>(s + o_last);
+  P.counters = reinterpret_cast<unsigned*>(s + o_cnt);
+  P.d2t_first = reinterpret_cast<int32_t*>(s + o_first);
   const size_t blocks = static_cast<size_t>(P.B) * nseg;
   if (blocks > INT32_MAX) return SV_ERR_UNSUPPORTED;
-  if (cudaMemsetAsync(P.counters, 0, static_cast<size_t>(P.B) * sizeof(unsigned), stream) != cudaSuccess)
+  const bool table = P.t2d != nullptr && P.d2t != nullptr && P.G > 0;
+  if (!table) P.d2t = nullptr;
+  const size_t smem = table ? static_cast<size_t>(NC) * kDChunk * sizeof(float) : 0;
+  auto kern = table ? decide_kernel<ET, ED, NC, true> : decide_kernel<ET, ED, NC, false>;
+  if (table && !cache.ensure(reinterpret_cast<const void*>(kern), smem, false)) return SV_ERR_CUDA;
+  if (cudaMemsetAsync(P.counters, 0, (static_cast<size_t>(P.B) + 1) * sizeof(unsigned), stream) != cudaSuccess)
     return SV_ERR_CUDA;
-  decide_kernel<ET, ED, NC><<<static_cast<unsigned>(blocks), kDThreads, 0, stream>>>(P, nseg);
+  if (table) {
+    const int n = std::max(P.Vd, nseg + 1);
+    d2t_range_kernel<<<(n + 255) / 256, 256, 0, stream>>>(P.d2t, P.Vd, P.V, NC * kDChunk, nseg, P.d2t_first,
+                                                          P.counters + P.B);
+    if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
+    note_launch(stream);
+  }
+  kern<<<static_cast<unsigned>(blocks), kDThreads, smem, stream>>>(P, nseg);
   if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
   note_launch(stream);
   return SV_OK;

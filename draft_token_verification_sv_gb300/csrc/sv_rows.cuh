@@ -202,15 +202,19 @@ struct DecideParams {
   const int32_t* ids;
   const float* u_resample;
   const int32_t* t2d;
+  const int32_t* d2t;       // with t2d: draft id -> target id
   int32_t* out_tokens;
   int32_t* num_accepted;
   int32_t* row_status;
   float* out_prob;
   // Scratch, set by launch_decide: per-chunk draw-weight sums, the last id
-  // with a positive weight per block, finished blocks per row.
+  // with a positive weight per block, finished blocks per row ([B], then one
+  // word counting the d2t entries that break the draft-range table), and
+  // per segment the first draft id whose target id lies in it or beyond.
   float* chunk_sums;
   int32_t* seg_last;
   unsigned* counters;
+  int32_t* d2t_first;
 };
 
 // The decision/draw pass with `scratch` of decide_scratch_bytes(B, V) bytes.

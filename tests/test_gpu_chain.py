@@ -147,6 +147,26 @@ def test_d2t_small(sv, shuffled, ties):
     compare_chain(got, want, ids, "f32")
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_d2t_sparse_segments(sv, dtype):
+    """A sorted d2t whose ids cluster in a few places of the target
+    vocabulary (most draw segments hold no draft id, one holds them densely),
+    with some draft logits at -inf: the draw's contiguous draft ranges."""
+    x = _case(70000, 5, dtype, 1.0, 0.9, ties=False, B=12, seed=31, d2t_frac=0.05)
+    Vd = x["draft"].shape[-1]
+    g = np.random.default_rng(7)
+    picks = np.concatenate([np.arange(0, 900), np.arange(40000, 40000 + 2000),
+                            g.choice(np.arange(60000, 70000), Vd - 2900, replace=False)])
+    x["d2t"] = np.sort(picks).astype(np.int32)
+    x["draft"][:, :, ::17] = -np.inf
+    x["draft_store"] = synth.to_bf16_bits(x["draft"]) if dtype == "bf16" else x["draft"]
+    ids = oracle_draft_ids(x)
+    got = run_chain(sv, x, ids)
+    want = oracle_chain(x, ids)
+    compare_chain(got, want, ids, dtype)
+    assert (got["num_accepted"] < 5).any()   # some rows draw from the residual
+
+
 def test_q_equals_p_accepts_everything(sv):
     x = _case(5000, 6, "bf16", 0.8, 0.9, ties=False, B=32, seed=11)
     x["draft"] = x["target"][:, :6].copy()
