@@ -104,6 +104,26 @@ def test_large_tie_group_at_cut(sv):
         _check(sv, rows, "f32", 1.0, top_p)
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_slice_cuts_far_from_the_row_cut(sv, dtype):
+    """Rows where one stretch of logits sits far above the rest: the other
+    slices' own cuts lie far from the row's, so where they hold logits in the
+    row's cut bin those are read by the rescan; plus rows where one slice is
+    far below the rest (its bins lie under the row's window)."""
+    g = np.random.default_rng(23)
+    V, R = 151936, 8
+    rows = g.normal(0, 1.5, (R, V)).astype(np.float32)
+    rows[0, 20000:40000] += 6.0
+    rows[1, :9000] += 4.0
+    rows[2, 100000:] -= 30.0
+    rows[3, 50000:60000] -= 80.0
+    rows[4, ::3] += 2.5
+    rows[5] = np.round(rows[5] * 4) / 4   # ties
+    rows[6, 70000:] = -np.inf
+    for T, top_p in ((1.0, 0.9), (0.6, 0.5), (2.0, 0.99)):
+        _check(sv, rows, dtype, T, top_p)
+
+
 def test_unaligned_rows(sv):
     """Rows whose start is not 16-byte aligned (odd row length, packed)."""
     g = np.random.default_rng(3)
