@@ -153,8 +153,7 @@ sv_status sv_verify_chain(const sv_chain_desc* desc, const void* target_logits,
 
 size_t sv_tree_workspace_size(const sv_tree_desc* desc) {
   if (!tree_desc_ok(desc)) return 0;
-  return tree_counter_bytes(desc->batch) +
-         align_up(static_cast<size_t>(desc->batch) * desc->nodes * sizeof(int32_t), 256);
+  return tree_greedy_layout(desc->batch, desc->nodes).total;
 }
 
 sv_status sv_verify_tree(const sv_tree_desc* desc, const void* logits, const int32_t* parents,

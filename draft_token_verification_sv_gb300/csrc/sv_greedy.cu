@@ -1,6 +1,11 @@
 // Greedy (temperature 0) verify: argmax of every target row, then the
 // per-group decision (chain prefix match or tree walk) by the last block of
-// the group to finish, all in one launch.
+// the group to finish, all in one launch.  One block streams a whole row
+// when there are enough rows to fill the GPU; for small batches a row is cut
+// into segments (one block each) so that every SM gets work: each segment
+// block folds its packed (value, lowest index) maximum into the row's word
+// with a 64-bit atomicMax, and the row's last segment block goes on with the
+// row's result.
 //
 // Sources: "SSD: extending the engine with new models and an EAGLE3 draft"
 // §七 (--temp 0 benchmarking); "A 2.16x speculative-decoding speedup from a
@@ -19,7 +24,10 @@ struct GreedyParams {
   int rows_per_group;  // γ+1 (chain), N (tree), 1 (sample)
   int groups;
   int32_t* g;          // [rows] argmax per row, -1 for a row with no finite logit
-  unsigned int* counters;  // [groups], zero between calls
+  unsigned int* counters;  // [groups], zero before the launch
+  int nseg;                // segment blocks per row
+  unsigned long long* rowmax;  // [rows] packed row maxima (nseg > 1), zero before the launch
+  unsigned int* segcnt;        // [rows] finished segment blocks (nseg > 1), zero before the launch
   // chain
   const int32_t* draft_ids;
   int32_t* out_tokens;
@@ -39,25 +47,31 @@ struct GreedyParams {
 
 // Largest value with the lowest index over one row, packed (see argmax_pack);
 // the result is valid in every thread.
+// Segment `seg` of `nseg` covers an equal share of whole loop steps
+// (THREADS * UNROLL 16-byte vectors) of the body, the last one to the end of
+// the row; segment 0 adds the scalar head and the last segment the tail.
 template <typename E, int THREADS, int UNROLL>
-__device__ __forceinline__ unsigned long long row_argmax(const E* row, int V,
+__device__ __forceinline__ unsigned long long row_argmax(const E* row, int V, int seg, int nseg,
                                                          unsigned long long* scratch) {
   constexpr int EPV = Elem<E>::kPerVec;
+  constexpr int kStep = THREADS * UNROLL;
   const RowSplit rs = split_row(row, V);
-  const int nvec = rs.nvec;
+  const int per_seg = ((rs.nvec + kStep - 1) / kStep + nseg - 1) / nseg;  // steps per segment
+  const int v_lo = min(rs.nvec, seg * per_seg * kStep);
+  const int nvec = seg == nseg - 1 ? rs.nvec : min(rs.nvec, v_lo + per_seg * kStep);
   const uint4* vp = reinterpret_cast<const uint4*>(row + rs.head);
   float bv = -CUDART_INF_F;
   int bi = 0x7fffffff;
   // Each thread visits its ids in increasing order (head, body, tail), so a
   // strict '>' keeps the lowest id among equal values.
-  if (static_cast<int>(threadIdx.x) < rs.head) {
+  if (seg == 0 && static_cast<int>(threadIdx.x) < rs.head) {
     const float x = Elem<E>::load(row + threadIdx.x);
     if (x > bv) {
       bv = x;
       bi = threadIdx.x;
     }
   }
-  for (int v0 = threadIdx.x; v0 < nvec; v0 += THREADS * UNROLL) {
+  for (int v0 = v_lo + static_cast<int>(threadIdx.x); v0 < nvec; v0 += kStep) {
     uint4 buf[UNROLL];
 #pragma unroll
     for (int u = 0; u < UNROLL; ++u) {
@@ -82,7 +96,7 @@ __device__ __forceinline__ unsigned long long row_argmax(const E* row, int V,
     }
   }
   const int tail = rs.tail0 + static_cast<int>(threadIdx.x);
-  if (tail < V) {
+  if (seg == nseg - 1 && tail < V) {
     const float x = Elem<E>::load(row + tail);
     if (x > bv) {
       bv = x;
@@ -234,10 +248,23 @@ __device__ void tree_walk(const GreedyParams& P, int b) {
 template <typename E, int THREADS, int UNROLL, GreedyMode MODE>
 __global__ void __launch_bounds__(THREADS) greedy_kernel(GreedyParams P) {
   __shared__ unsigned long long s_red[32];
-  __shared__ bool s_last;
-  const int row = blockIdx.x;
+  __shared__ bool s_seg_last, s_last;
+  const int row = blockIdx.x / P.nseg;
+  const int seg = blockIdx.x - row * P.nseg;
   const E* rp = reinterpret_cast<const E*>(P.logits) + static_cast<int64_t>(row) * P.stride;
-  const unsigned long long best = row_argmax<E, THREADS, UNROLL>(rp, P.V, s_red);
+  unsigned long long best = row_argmax<E, THREADS, UNROLL>(rp, P.V, seg, P.nseg, s_red);
+  if (P.nseg > 1) {
+    // Fold into the row's maximum; the row's last segment block goes on.
+    if (threadIdx.x == 0) {
+      atomicMax(P.rowmax + row, best);
+      __threadfence();
+      s_seg_last = atomicAdd(P.segcnt + row, 1u) == static_cast<unsigned>(P.nseg - 1);
+    }
+    __syncthreads();
+    if (!s_seg_last) return;
+    __threadfence();
+    best = __ldcg(P.rowmax + row);
+  }
   const bool empty = (best >> 32) == static_cast<unsigned long long>(order_key(-CUDART_INF_F));
   const int idx = empty ? -1 : argmax_index(best);
   if constexpr (MODE == GreedyMode::kSample) {
@@ -253,7 +280,6 @@ __global__ void __launch_bounds__(THREADS) greedy_kernel(GreedyParams P) {
       __threadfence();
       const unsigned int prev = atomicAdd(P.counters + group, 1u);
       s_last = prev == static_cast<unsigned int>(P.rows_per_group - 1);
-      if (s_last) P.counters[group] = 0u;  // leave the workspace zeroed
     }
     __syncthreads();
     if (!s_last) return;
@@ -263,12 +289,37 @@ __global__ void __launch_bounds__(THREADS) greedy_kernel(GreedyParams P) {
   }
 }
 
+constexpr int kGThreads = 512;
+constexpr int kGUnroll = 8;
+
+// Segment blocks per row: 1 when the rows alone give every SM two blocks
+// (measured: splitting rows then only adds the per-block reduction and
+// atomics), else up to one segment per loop step so that small batches
+// still spread over the GPU.
+template <typename E>
+static int greedy_segments(int rows, int V) {
+  static std::atomic<int> sms[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+  int n = sms[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    sms[dev].store(n, std::memory_order_relaxed);
+  }
+  const long long want = 2LL * n;
+  if (rows <= 0 || rows >= want) return 1;
+  constexpr int step = kGThreads * kGUnroll;
+  const int max_seg = std::max(1, V / Elem<E>::kPerVec / step);
+  return static_cast<int>(std::min<long long>(max_seg, (want + rows - 1) / rows));
+}
+
+// rows x nseg blocks; P.counters, P.rowmax and P.segcnt zeroed by the caller.
 template <typename E, GreedyMode MODE>
 static sv_status launch_greedy(const GreedyParams& P, int rows, cudaStream_t stream) {
-  constexpr int kThreads = 512;
-  constexpr int kUnroll = 8;
   if (rows == 0) return SV_OK;
-  greedy_kernel<E, kThreads, kUnroll, MODE><<<rows, kThreads, 0, stream>>>(P);
+  const long long blocks = static_cast<long long>(rows) * P.nseg;
+  if (blocks > INT32_MAX) return SV_ERR_UNSUPPORTED;
+  greedy_kernel<E, kGThreads, kGUnroll, MODE><<<static_cast<unsigned>(blocks), kGThreads, 0, stream>>>(P);
   if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
   note_launch(stream);
   return SV_OK;
@@ -285,12 +336,20 @@ sv_status greedy_chain(const sv_chain_desc& d, const void* target, const int32_t
   P.rows_per_group = d.gamma + 1;
   P.groups = d.batch;
   WorkspaceLayout L = chain_workspace_layout(d);
-  P.counters = reinterpret_cast<unsigned int*>(static_cast<char*>(workspace) + L.counters);
-  // The workspace is scratch shared with other calls: clear the counters.
+  char* ws = static_cast<char*>(workspace);
+  P.counters = reinterpret_cast<unsigned int*>(ws + L.counters);
+  // The row maxima and segment counters live in the statistics region,
+  // which the greedy path does not otherwise use (12 bytes per row against
+  // 32 per statistics row).
+  P.nseg = d.target_dtype == SV_BF16 ? greedy_segments<uint16_t>(rows, d.vocab) : greedy_segments<float>(rows, d.vocab);
+  P.rowmax = reinterpret_cast<unsigned long long*>(ws + L.stats);
+  P.segcnt = reinterpret_cast<unsigned int*>(ws + L.stats + static_cast<size_t>(rows) * sizeof(unsigned long long));
+  // The workspace is scratch shared with other calls: clear the counters
+  // (and the row maxima) in one go.
   start_phases(stream);
-  if (cudaMemsetAsync(P.counters, 0, static_cast<size_t>(d.batch) * sizeof(uint32_t), stream) != cudaSuccess)
-    return SV_ERR_CUDA;
-  P.g = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + L.argmax);
+  const size_t clear = P.nseg > 1 ? L.stats + static_cast<size_t>(rows) * 12 : static_cast<size_t>(d.batch) * 4;
+  if (cudaMemsetAsync(ws, 0, clear, stream) != cudaSuccess) return SV_ERR_CUDA;
+  P.g = reinterpret_cast<int32_t*>(ws + L.argmax);
   P.draft_ids = ids;
   P.out_tokens = out_tokens;
   P.num_accepted = num_accepted;
@@ -311,11 +370,18 @@ sv_status greedy_tree(const sv_tree_desc& d, const void* logits, const int32_t* 
   P.V = d.vocab;
   P.rows_per_group = d.nodes;
   P.groups = d.batch;
-  P.counters = static_cast<unsigned int*>(workspace);
+  const int rows = d.batch * d.nodes;
+  const TreeGreedyLayout TL = tree_greedy_layout(d.batch, d.nodes);
+  char* ws = static_cast<char*>(workspace);
+  P.counters = reinterpret_cast<unsigned int*>(ws);
+  P.nseg = d.dtype == SV_BF16 ? greedy_segments<uint16_t>(rows, d.vocab) : greedy_segments<float>(rows, d.vocab);
+  P.segcnt = reinterpret_cast<unsigned int*>(ws + TL.segcnt);
+  P.rowmax = reinterpret_cast<unsigned long long*>(ws + TL.rowmax);
   start_phases(stream);
-  if (cudaMemsetAsync(P.counters, 0, static_cast<size_t>(d.batch) * sizeof(uint32_t), stream) != cudaSuccess)
-    return SV_ERR_CUDA;
-  P.g = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + tree_counter_bytes(d.batch));
+  // Counters, segment counters and row maxima are contiguous: one clear.
+  const size_t clear = P.nseg > 1 ? TL.g : static_cast<size_t>(d.batch) * sizeof(uint32_t);
+  if (cudaMemsetAsync(ws, 0, clear, stream) != cudaSuccess) return SV_ERR_CUDA;
+  P.g = reinterpret_cast<int32_t*>(ws + TL.g);
   P.parents = parents;
   P.tokens = tokens;
   P.accept_len = accept_len;
@@ -323,7 +389,6 @@ sv_status greedy_tree(const sv_tree_desc& d, const void* logits, const int32_t* 
   P.out_tokens = out_tokens;
   P.row_status = row_status;
   P.max_depth = d.max_depth;
-  const int rows = d.batch * d.nodes;
   return d.dtype == SV_BF16 ? launch_greedy<uint16_t, GreedyMode::kTree>(P, rows, stream)
                             : launch_greedy<float, GreedyMode::kTree>(P, rows, stream);
 }
@@ -336,6 +401,7 @@ sv_status greedy_sample(const sv_sample_desc& d, const void* logits, int32_t* ou
   P.V = d.vocab;
   P.rows_per_group = 1;
   P.groups = d.rows;
+  P.nseg = 1;  // no workspace: whole rows
   P.out_tokens = out_tokens;
   P.out_prob = out_prob;
   return d.dtype == SV_BF16 ? launch_greedy<uint16_t, GreedyMode::kSample>(P, d.rows, stream)

@@ -88,6 +88,21 @@ inline size_t tree_counter_bytes(int batch) {
   return align_up(static_cast<size_t>(batch) * sizeof(uint32_t), 256);
 }
 
+// Greedy tree workspace: [group counters: B u32][segment counters: B*N u32]
+// [row maxima: B*N u64][argmax: B*N i32]; the first three are cleared per call.
+struct TreeGreedyLayout {
+  size_t segcnt, rowmax, g, total;
+};
+inline TreeGreedyLayout tree_greedy_layout(int batch, int nodes) {
+  const size_t rows = static_cast<size_t>(batch) * static_cast<size_t>(nodes);
+  TreeGreedyLayout L{};
+  L.segcnt = tree_counter_bytes(batch);
+  L.rowmax = L.segcnt + align_up(rows * sizeof(uint32_t), 256);
+  L.g = L.rowmax + align_up(rows * sizeof(unsigned long long), 256);
+  L.total = L.g + align_up(rows * sizeof(int32_t), 256);
+  return L;
+}
+
 // Entry points of the individual paths (arguments already validated).
 sv_status greedy_chain(const sv_chain_desc& d, const void* target, const int32_t* ids,
                        int32_t* out_tokens, int32_t* num_accepted, float* p_draft, float* q_draft,

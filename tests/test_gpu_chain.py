@@ -137,6 +137,27 @@ def test_small_shapes_greedy(sv, V, G, dtype):
     assert np.array_equal(got["num_accepted"], want["num_accepted"])
 
 
+@pytest.mark.parametrize("dtype,V,B", [("bf16", 128256, 1), ("f32", 151936, 2), ("bf16", 200003, 3)])
+def test_greedy_small_batch_long_rows(sv, dtype, V, B):
+    """Few long rows: each row is split over several blocks (segments whose
+    maxima meet in one 64-bit word); ties and the winner planted in the
+    scalar tail and at a segment boundary."""
+    G = 4
+    x = _case(V, G, dtype, 0.0, 1.0, ties=True, B=B, seed=V + B)
+    t = x["target"]
+    t[0, 0, :] = np.round(t[0, 0, :])
+    t[0, 0, V - 1] = 50.0                      # the scalar tail (V not a multiple of 8 here or there)
+    t[0, 1, 4096 * 8 - 1: 4096 * 8 + 1] = 60.0  # equal maxima on both sides of a segment boundary
+    x["target_store"] = synth.to_bf16_bits(t) if dtype == "bf16" else t
+    x["target"] = synth.bf16_bits_to_f32(x["target_store"]) if dtype == "bf16" else t
+    ids = oracle_draft_ids(x)
+    ids[:, 0] = np.argmax(x["target"][:, 0, :], axis=-1)   # accept the first draft
+    got = run_chain(sv, x, ids)
+    want = oracle_chain(x, ids)
+    assert np.array_equal(got["tokens"], want["tokens"])
+    assert np.array_equal(got["num_accepted"], want["num_accepted"])
+
+
 @pytest.mark.parametrize("shuffled", [False, True])
 @pytest.mark.parametrize("ties", [False, True])
 def test_d2t_small(sv, shuffled, ties):

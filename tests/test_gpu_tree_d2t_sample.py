@@ -64,6 +64,20 @@ def test_tree_small_with_ties(sv, N, V, D, dtype):
     _tree_compare(got, want)
 
 
+@pytest.mark.parametrize("dtype,V", [("bf16", 128256), ("f32", 151936)])
+def test_tree_one_tree_long_rows(sv, dtype, V):
+    """One small tree over a large vocabulary: its rows are split over
+    several blocks each."""
+    cfg = synth.TreeConfig("t", 1, 6, V, dtype, 3, 8, 2.0, 0.8, 0.0)
+    tr = synth.make_tree_inputs(cfg, seed=V)
+    for n in range(1, 6):
+        if n % 2:
+            tr["tokens"][0, n] = int(np.argmax(tr["logits"][0, tr["parents"][0, n]]))
+    got = _tree_run(sv, tr, dtype)
+    want = O.verify_tree(tr["logits"], tr["parents"], tr["tokens"], tr["max_depth"])
+    _tree_compare(got, want)
+
+
 def test_tree_invalid(sv):
     tr = synth.make_tree_inputs(synth.TREE, batch=4, vocab=257)
     tr["parents"][1, 5] = 9          # parent after child
