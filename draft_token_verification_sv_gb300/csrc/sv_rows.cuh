@@ -64,6 +64,7 @@ struct StatsLaunch {
   float top_p;
   int nslices[2];      // top-p kernel: slices per row of each set
   float* summ;         // top-p kernel: per-slice summaries
+  uint8_t* codes;      // top-p kernel: every logit's bin under its slice maximum, one byte each
   unsigned* counters;  // top-p kernel: finished slices per row
   DecideIn dec;
 };

@@ -100,9 +100,11 @@ struct ToppShared {
   float xlo, xhi;
 };
 
-// L2 eviction priorities: the slice pass marks a row's lines evict-last so
-// they survive until the row's last block rescans them; the rescan marks
-// them evict-first once used.  Hints only: results do not depend on them.
+// L2 eviction priorities: the slice pass reads the logits evict-first (they
+// are read again only where a row falls back to the value scan, or for the
+// few logits of the cut bin) and writes the code bytes evict-last, so they
+// survive until the row's last block reads and drops them.  Hints only:
+// results do not depend on them.
 __device__ __forceinline__ uint64_t l2_policy_evict_last() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
@@ -112,6 +114,13 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
   return p;
+}
+__device__ __forceinline__ void stg_hint(uint32_t* a, uint32_t v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.u32 [%0], %1, %2;" ::"l"(a), "r"(v), "l"(pol) : "memory");
+}
+__device__ __forceinline__ void stg_hint(uint2* a, uint2 v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.v2.u32 [%0], {%1, %2}, %3;" ::"l"(a), "r"(v.x), "r"(v.y), "l"(pol)
+               : "memory");
 }
 __device__ __forceinline__ uint4 ldg_hint(const uint4* a, uint64_t pol) {
   uint4 r;
@@ -511,6 +520,102 @@ __device__ __forceinline__ int collect_ids(ToppShared& sh, const E* row, int len
   return wn;
 }
 
+// Ids of the logits of the cut bin into this warp's region of sh.cand.j,
+// found by the slices' code bytes instead of their values: in slice q the
+// logits of the cut bin are those whose code equals tq[q] (>= 0; -1: the
+// slice has none; every slice's cut bin lies above its lowest bin).  Sixteen
+// codes per 16-byte load, four compared at once (a byte of w ^ t is zero
+// exactly where the code matches); the scalar head and tail logits are
+// compared by value.  The codes are dropped from L2 afterwards (they are
+// never needed again).  Returns the warp's count, which may exceed the
+// region (entries past it are dropped).  Block-wide.
+template <typename E>
+__device__ __forceinline__ int collect_codes(ToppShared& sh, const uint8_t* codes, const int* tq, int ns,
+                                             const E* row, int len, float xlo, float xhi) {
+  constexpr int SL = SliceShape<E>::kEPT * kSThreads;  // logits (code bytes) per slice
+  constexpr int Q16 = SL / 16;                           // 16-byte code vectors per slice
+  static_assert((Q16 & (Q16 - 1)) == 0, "slices of a power-of-two size");
+  constexpr int kQShift = Q16 == 512 ? 9 : 10;
+  static_assert((1 << kQShift) == Q16, "shift of the slice index");
+  constexpr int U = 2;  // code vectors per thread per batch
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  int* region = sh.cand.j + warp * kRegion;
+  const RowSplit rs = split_row(row, len);
+  const uint4* c4 = reinterpret_cast<const uint4*>(codes);
+  const int total = ns * Q16;
+  int wn = 0;
+  for (int g0 = 0; g0 < total; g0 += U * kSThreads) {
+    uint4 cv[U];
+    int t[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int g = g0 + u * kSThreads + tid;
+      t[u] = g < total ? tq[g >> kQShift] : -1;
+      cv[u] = t[u] >= 0 ? __ldcg(c4 + g) : make_uint4(0u, 0u, 0u, 0u);
+    }
+    // Zero-byte masks of w ^ t: the top bit of each matching byte.
+    uint32_t mk[U][4];
+    int cnt = 0;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const uint32_t t4 = t[u] >= 0 ? static_cast<uint32_t>(t[u]) * 0x01010101u : 0u;
+      const uint32_t w[4] = {cv[u].x, cv[u].y, cv[u].z, cv[u].w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t x4 = w[i] ^ t4;
+        mk[u][i] = t[u] >= 0 ? ~(((x4 & 0x7f7f7f7fu) + 0x7f7f7f7fu) | x4 | 0x7f7f7f7fu) : 0u;
+        cnt += __popc(mk[u][i]);
+      }
+    }
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    int slot = wn + incl - cnt;
+    if (cnt) {
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int g = g0 + u * kSThreads + tid;
+        const int q = g >> kQShift;
+        const int off = (g & (Q16 - 1)) * 16;  // first code of the vector within slice q
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          uint32_t m = mk[u][i];
+          while (m) {
+            const int bit = __ffs(m) - 1;
+            m &= m - 1;
+            if (slot < kRegion) region[slot] = rs.head + q * SL + off + 4 * i + (bit >> 3);
+            ++slot;
+          }
+        }
+      }
+    }
+    wn += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  // The scalar head and tail logits, by value.
+  const unsigned lane_lt = (1u << lane) - 1u;
+  const int ntail = len - rs.tail0;
+  for (int t0 = 0; t0 < rs.head + ntail; t0 += kSThreads) {
+    const int t = t0 + tid;
+    const int j = t < rs.head ? t : (t < rs.head + ntail ? rs.tail0 + (t - rs.head) : -1);
+    const float x = j >= 0 ? Elem<E>::load(row + j) : -CUDART_INF_F;
+    const bool cand = x >= xlo && x < xhi;
+    const unsigned bal = __ballot_sync(0xffffffffu, cand);
+    const int slot = wn + __popc(bal & lane_lt);
+    if (cand && slot < kRegion) region[slot] = j;
+    wn += __popc(bal);
+  }
+  // Drop the codes from L2 without writing them back (128-byte lines; every
+  // slice's codes start on a 128-byte boundary), once every warp has read
+  // them.
+  __syncthreads();
+  for (int i = tid; i < total / 8; i += kSThreads)
+    asm volatile("discard.global.L2 [%0], 128;" ::"l"(c4 + 8 * i) : "memory");
+  return wn;
+}
+
 // The cut among the candidates of the cut bin (n <= kCandCap, in
 // sh.cand): radix levels over their order keys, each keeping the digit where
 // the mass from the top first exceeds the limit (counts and fixed-point
@@ -701,6 +806,31 @@ __device__ void resolve_candidates(ToppShared& sh, const RowSet& S, float c, flo
   }
 }
 
+// Bin every logit of this thread's vectors with add (which returns the
+// logit's bin) and store the bins as bytes in logit order: vector k of
+// thread tid holds logits (k * kSThreads + tid) * EPV + 0..EPV-1 of the slice.
+template <typename E, int VPT, typename F>
+__device__ __forceinline__ void bin_vectors(const uint4 (&raw)[VPT], uint8_t* codes, F&& add) {
+  constexpr int EPV = Elem<E>::kPerVec;
+  const int tid = threadIdx.x;
+  const uint64_t keep = l2_policy_evict_last();
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) {
+    uint32_t w[EPV / 4];
+#pragma unroll
+    for (int h = 0; h < EPV / 4; ++h) {
+      w[h] = 0u;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) w[h] |= add(Elem<E>::at(raw[k], 4 * h + j)) << (8 * j);
+    }
+    if constexpr (EPV == 4) {
+      stg_hint(reinterpret_cast<uint32_t*>(codes) + k * kSThreads + tid, w[0], keep);
+    } else {
+      stg_hint(reinterpret_cast<uint2*>(codes) + k * kSThreads + tid, make_uint2(w[0], w[1]), keep);
+    }
+  }
+}
+
 template <typename E>
 __global__ void __launch_bounds__(kSThreads, 5) topp_slice_kernel(StatsLaunch L) {
   constexpr int EPV = Elem<E>::kPerVec;
@@ -730,16 +860,15 @@ __global__ void __launch_bounds__(kSThreads, 5) topp_slice_kernel(StatsLaunch L)
 #pragma unroll
   for (int i = 0; i < kWarps * kNB / kSThreads; ++i) (&sh.wh[0][0])[i * kSThreads + tid] = 0u;
 
-  // 1. The slice in registers; slice maximum.  Evict-last in L2: the row's
-  // last block rescans it from L2.
+  // 1. The slice in registers; slice maximum.
   const RowSplit rs = split_row(row, S.len);
   const uint4* vp = reinterpret_cast<const uint4*>(row + rs.head);
-  const uint64_t keep = l2_policy_evict_last();
+  const uint64_t once = l2_policy_evict_first();
   uint4 raw[VPT];
 #pragma unroll
   for (int k = 0; k < VPT; ++k) {
     const int v = s * VPS + k * kSThreads + tid;
-    raw[k] = v < rs.nvec ? ldg_hint(vp + v, keep) : Elem<E>::neg_inf_vec();
+    raw[k] = v < rs.nvec ? ldg_hint(vp + v, once) : Elem<E>::neg_inf_vec();
   }
   float xv = -CUDART_INF_F;
   if (s == 0) {
@@ -773,6 +902,9 @@ __global__ void __launch_bounds__(kSThreads, 5) topp_slice_kernel(StatsLaunch L)
   // logits are counted in the lowest bin with their mass relative to its
   // edge (they round to 0 more than 21 octaves below it, and are skipped);
   // the merge never resolves a cut inside that bin (exact path instead).
+  // Every logit's bin t = Gs - fy (255: the lowest bin or below) also goes
+  // to this slice's code bytes, in the order of the logits.
+  uint8_t* codes = L.codes + static_cast<int64_t>(sbase + s) * (VPS * EPV);
   const bool live = ms > -CUDART_INF_F;
   const float Gsf = live ? floorf(ms * c8) : 0.0f;
   const float bottom = Gsf - static_cast<float>(kNB - 1);
@@ -784,7 +916,7 @@ __global__ void __launch_bounds__(kSThreads, 5) topp_slice_kernel(StatsLaunch L)
     // out of the mantissa bits.
     const uint32_t whs = static_cast<uint32_t>(__cvta_generic_to_shared(wh));
     const float gm = Gsf + kMagicFloor;
-    auto add = [&](float x) {
+    auto add = [&](float x) -> uint32_t {
       const float fy = fmaxf(__fadd_rd(x * c8, kMagicFloor) - kMagicFloor, bottom);
       // l*c - (f+1)/8 (in [-1/8, 0] inside the window): the mass relative to
       // the bin's upper edge.
@@ -792,25 +924,22 @@ __global__ void __launch_bounds__(kSThreads, 5) topp_slice_kernel(StatsLaunch L)
       const uint32_t v = __float_as_uint(fmaf(ex2(t), SliceShape<E>::kFix, kMagicRound)) - kMagicRoundBits;
       const uint32_t idx = __float_as_uint(gm - fy) - kMagicFloorBits;
       asm volatile("red.shared.add.u32 [%0], %1;" ::"r"(whs + idx * 4u), "r"(v) : "memory");
+      return idx;
     };
-#pragma unroll
-    for (int k = 0; k < VPT; ++k)
-#pragma unroll
-      for (int i = 0; i < EPV; ++i) add(Elem<E>::at(raw[k], i));
+    bin_vectors<E, VPT>(raw, codes, add);
     if (xv > -CUDART_INF_F) add(xv);
   } else if (live) {
     // Logits too large for the magic additions: the same bins by floorf and
     // conversions.
-    auto add = [&](float x) {
+    auto add = [&](float x) -> uint32_t {
       const float fy = fmaxf(floorf(x * c8), bottom);
       const float t = fmaf(x, c, fmaf(fy, -0.125f, -0.125f));
       const unsigned v = __float2uint_rn(ex2(t) * SliceShape<E>::kFix);
-      if (v) atomicAdd(&wh[static_cast<int>(Gsf - fy)], v);
+      const int idx = static_cast<int>(Gsf - fy);
+      if (v) atomicAdd(&wh[idx], v);
+      return static_cast<uint32_t>(idx);
     };
-#pragma unroll
-    for (int k = 0; k < VPT; ++k)
-#pragma unroll
-      for (int i = 0; i < EPV; ++i) add(Elem<E>::at(raw[k], i));
+    bin_vectors<E, VPT>(raw, codes, add);
     if (xv > -CUDART_INF_F) add(xv);
   }
   __syncthreads();
@@ -940,9 +1069,27 @@ __global__ void __launch_bounds__(kSThreads, 5) topp_slice_kernel(StatsLaunch L)
         sh.xlo = first_at_or_above(Bf, c8);
         sh.xhi = first_at_or_above(Bf + 1.0f, c8);
       }
+      // The cut bin as a code of each slice (in hcnt, free until the
+      // resolution); a slice whose lowest bin holds the cut bin (or rows of
+      // more slices than the table holds) sends the row to the value scan.
+      int* tq = reinterpret_cast<int*>(sh.hcnt);
+      if (tid == 0) sh.ncand = ns > kNB;
+      __syncthreads();
+      for (int q = tid; q < ns && q < kNB; q += kSThreads) {
+        int t = -1;
+        const float mq = staged ? hm[q] : __ldcg(sum0 + static_cast<int64_t>(q) * kSummary);
+        if (mq > -CUDART_INF_F) {
+          const float Gq = staged ? hg[q] : __ldcg(sum0 + static_cast<int64_t>(q) * kSummary + 2);
+          t = gstar - static_cast<int>(Grf - Gq);
+          if (t >= kNB - 1) sh.ncand = 1;
+        }
+        tq[q] = t;
+      }
       __syncthreads();
       const float xlo = sh.xlo, xhi = sh.xhi;
-      const int wn = collect_ids<E>(sh, row, S.len, xlo, xhi);
+      const int wn = sh.ncand ? collect_ids<E>(sh, row, S.len, xlo, xhi)
+                              : collect_codes<E>(sh, L.codes + static_cast<int64_t>(sbase) * (VPS * EPV), tq, ns,
+                                                 row, S.len, xlo, xhi);
       if (lane == 0) sh.wcnt[warp] = wn;
       __syncthreads();
       int total_c = 0, my_off = 0, over = 0;
@@ -1058,10 +1205,17 @@ static sv_status launch_typed(const StatsLaunch& L, cudaStream_t stream) {
 static int slices_of(int len, int slice) { return len <= 0 ? 1 : (len + slice - 1) / slice; }
 int topp_slices(int len) { return slices_of(len, kMinSlice); }
 
+// Code bytes: one per logit of every slice, slices padded to whole slices.
+// An upper bound from the count of kMinSlice-logit slices: two more such
+// slices per row cover the rows cut into the larger bf16 slices.
+static size_t topp_code_bytes_bound(size_t slices, int rows) {
+  return (slices + 2 * static_cast<size_t>(rows)) * static_cast<size_t>(kMinSlice);
+}
+
 size_t topp_scratch_bytes(int rows0, int len0, int rows1, int len1) {
   const size_t slices = static_cast<size_t>(rows0) * topp_slices(len0) + static_cast<size_t>(rows1) * topp_slices(len1);
   // Slack for the alignment of two separately launched sets.
-  return align_up(slices * kSummary * sizeof(float), 256) +
+  return align_up(slices * kSummary * sizeof(float), 256) + align_up(topp_code_bytes_bound(slices, rows0 + rows1), 256) +
          align_up(static_cast<size_t>(rows0 + rows1) * sizeof(unsigned), 256) + 512;
 }
 
@@ -1073,8 +1227,11 @@ sv_status launch_topp_stats(StatsLaunch L, sv_dtype dtype, void* scratch, cudaSt
   const size_t slices = static_cast<size_t>(L.set[0].rows) * L.nslices[0] +
                         (L.nsets > 1 ? static_cast<size_t>(L.set[1].rows) * L.nslices[1] : 0);
   L.summ = static_cast<float*>(scratch);
+  // The layout for these slices (within topp_scratch_bytes' bound).
+  L.codes = reinterpret_cast<uint8_t*>(static_cast<char*>(scratch) + align_up(slices * kSummary * sizeof(float), 256));
   L.counters = reinterpret_cast<unsigned*>(static_cast<char*>(scratch) +
-                                           align_up(slices * kSummary * sizeof(float), 256));
+                                           align_up(slices * kSummary * sizeof(float), 256) +
+                                           align_up(slices * static_cast<size_t>(slice), 256));
   if (cudaMemsetAsync(L.counters, 0, static_cast<size_t>(rows) * sizeof(unsigned), stream) != cudaSuccess)
     return SV_ERR_CUDA;
   return dtype == SV_BF16 ? launch_typed<uint16_t>(L, stream) : launch_typed<float>(L, stream);
