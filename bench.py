@@ -22,7 +22,8 @@ the smaller of its median event-timed duration and the median step time
 (both bound it from above).
 "e2e" is the same metric through the public Python call with the step's
 inputs copied from pinned host memory and its outputs copied back, every
-step.
+step; the copy of step i+1's inputs (on a copy stream, into a second device
+buffer) overlaps the verify of step i.
 """
 from __future__ import annotations
 
@@ -593,7 +594,9 @@ def run_e2e(cfg, inputs, sv, dev, stream, K, dist, path_walk=False, topk=0):
     if not tree and cfg.temperature == 0:
         names = ["target", "ids"]
     host = {n: inputs[n].cpu().pin_memory() for n in names}
-    devb = {n: torch.empty_like(inputs[n]) for n in names}
+    # Two device copies of the inputs: step i+1's inputs are copied (on a copy
+    # stream) while step i is verified; events order each buffer's reuse.
+    bufs = [{n: torch.empty_like(inputs[n]) for n in names} for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     L = cfg.max_depth + 1 if tree else cfg.gamma + 1
     if topk:
@@ -602,9 +605,20 @@ def run_e2e(cfg, inputs, sv, dev, stream, K, dist, path_walk=False, topk=0):
     k_host = torch.empty(cfg.batch, dtype=torch.int32).pin_memory()
     d2h = out_host.numel() * 4 + (0 if topk else k_host.numel() * 4)
 
-    def one():
-        for n in names:
-            devb[n].copy_(host[n], non_blocking=True)
+    copy_stream = torch.cuda.Stream(device=dev)
+    ready = [torch.cuda.Event() for _ in range(2)]
+    free = [torch.cuda.Event() for _ in range(2)]
+    for e in free:
+        e.record(stream)
+
+    def one(i):
+        devb = bufs[i % 2]
+        with torch.cuda.stream(copy_stream):
+            copy_stream.wait_event(free[i % 2])
+            for n in names:
+                devb[n].copy_(host[n], non_blocking=True)
+            ready[i % 2].record(copy_stream)
+        stream.wait_event(ready[i % 2])
         if topk:
             ids = sv.topk(devb["logits"].reshape(cfg.batch * cfg.nodes, cfg.vocab), topk)
             out_host.copy_(ids.reshape(cfg.batch, -1), non_blocking=True)
@@ -623,16 +637,18 @@ def run_e2e(cfg, inputs, sv, dev, stream, K, dist, path_walk=False, topk=0):
                                 t2d=inputs["t2d"], probs=False)
             out_host.copy_(o["tokens"], non_blocking=True)
             k_host.copy_(o["num_accepted"], non_blocking=True)
+        free[i % 2].record(stream)
 
     with torch.cuda.stream(stream):
-        for _ in range(3):
-            one()
-        stream.synchronize()
+        for i in range(3):
+            one(i)
+        torch.cuda.synchronize()
         dist.barrier()
         start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         start.record(stream)
-        for _ in range(K):
-            one()
+        copy_stream.wait_event(start)
+        for i in range(K):
+            one(i)
         end.record(stream)
     torch.cuda.synchronize()
     dist.barrier()
