@@ -707,15 +707,14 @@ def _share_host(host):
 
 
 def _worker_init(cfg, spec):
-    from multiprocessing import resource_tracker, shared_memory
+    from multiprocessing import shared_memory
     host, keep = {}, []
     for k, sp in spec.items():
         if sp[0] == "shm":
+            # The parent owns and unlinks the block; attaching registers the
+            # same name with the shared resource tracker again, which the
+            # parent's unlink then removes once.
             shm = shared_memory.SharedMemory(name=sp[1])
-            try:  # the parent owns (and unlinks) the block
-                resource_tracker.unregister(shm._name, "shared_memory")
-            except Exception:
-                pass
             keep.append(shm)
             host[k] = np.ndarray(sp[2], np.dtype(sp[3]), buffer=shm.buf)
         else:

@@ -88,6 +88,37 @@ def test_qwen3_d2t_full_size(sv, qwen3):
     _report("qwen3 d2t (sampled rows)", compare_chain(got, want, ids, "f32", rows=rows))
 
 
+def test_qwen3_d2t_every_batch_row(sv, qwen3):
+    """All 256 batch rows of the full workload against the oracle, which runs
+    one batch row per task on every host core: tokens and accept counts must
+    match, except in rows with an oracle decision within 1e-6 of its
+    threshold.  On 151936-id rows one logit near the top-p cut carries about
+    1e-6 to 1e-8 of the mass, so every row's cut is that close to top_p and
+    every row counts as near; the mismatches among them must stay rare (at
+    most 2% of the rows)."""
+    import bench
+    x, ids = qwen3
+    got = run_chain(sv, x, ids)
+    host = {"target": x["target"], "draft": x["draft"], "draft_ids": ids, "u_accept": x["u_accept"],
+            "u_resample": x["u_resample"], "d2t": x["d2t"]}
+    pool = bench.OraclePool(x["cfg"], host)
+    try:
+        done, _ = pool.rows(range(x["batch"]))
+    finally:
+        pool.close()
+    assert sorted(b for b, _, _ in done) == list(range(x["batch"]))
+    near = near_mis = 0
+    for b, want, margin in done:
+        same = np.array_equal(got["tokens"][b].astype(np.int64), want)
+        if margin < O.NEAR:
+            near += 1
+            near_mis += int(not same)
+        else:
+            assert same, (b, got["tokens"][b], want, margin)
+    print(f"[qwen3 d2t, all {len(done)} batch rows] near-threshold={near} near-threshold mismatches={near_mis}")
+    assert near_mis <= len(done) // 50, near_mis
+
+
 def test_qwen3_d2t_repeat_is_identical(sv, qwen3):
     """Two calls in a row give the same bits (deterministic, workspace reset)."""
     x, ids = qwen3
