@@ -22,10 +22,15 @@
 //
 // Launches: the statistics pass over every target and draft row (the
 // streaming kernel, or the top-p kernel when top_p < 1) gives each row its
-// exp2 offset, kept mass and top-p cut; then tree_sample_kernel, one block
-// per tree, walks from the root.  A pass keeps per-chunk sums of
+// exp2 offset, kept mass and top-p cut; then tree_sample_kernel walks each
+// tree from the root, one cluster of CS thread blocks per tree (CS = 2 when
+// the trees leave SMs idle, else 1).  A pass keeps per-chunk sums of
 // max(0, p - c q) in shared memory; the final inverse-CDF draw reuses them
-// and rescans only the chunk that holds u * total.
+// and rescans only the chunk that holds u * total.  In a cluster every block
+// runs the whole walk on the same data and takes the same decisions (the
+// same double-precision arithmetic in the same order); only a pass is split:
+// block r computes the chunks k = r (mod CS) and stores each chunk sum into
+// every block's shared memory, and a cluster barrier ends the pass.
 #include "sv_internal.h"
 #include "sv_rows.cuh"
 
@@ -89,9 +94,14 @@ struct TSShared {
   int first_child[SV_MAX_TREE_NODES];
   int next_sib[SV_MAX_TREE_NODES];
   int depth[SV_MAX_TREE_NODES];
+  // Node n's accept test as a child of its parent, for every n > 0 (the
+  // test does not depend on the path the walk takes): p(x_n) and q(x_n)
+  // under the parent's rows, and the node's uniform.
+  double test[SV_MAX_TREE_NODES][3];
   double chunk_sum[kTSMaxChunks];
   double red[32];
-  double pq[2];
+  double warp_before[32];  // the draw: prefix of the warps before each
+  double tile_total;
   RowDist pd[2];
   double bcast_d;
   int bcast_i;
@@ -170,11 +180,19 @@ __device__ __forceinline__ float chunk_residual(const NodeRows<E>& R, int j0, in
 // One pass over the node's rows: chunk_sum[k] = sum of max(0, p - cj q) over
 // chunk k (one warp per chunk, fp32 per lane, double across lanes); returns
 // the row total (double, the same in every thread).
-template <typename E>
+template <typename E, int CS>
 __device__ double residual_pass(const NodeRows<E>& R, const TreeSampleParams& P, Coef cj, TSShared& sh) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool filtered = (R.p.tau | R.q.tau) != 0u;
-  for (int k = warp; k < P.nchunks; k += kTSWarps) {
+  int rank = 0;
+  if constexpr (CS > 1) {
+    // No block writes into another's chunk sums before every block of the
+    // cluster is done reading the previous pass's (every block makes the
+    // same sequence of passes, so the barriers pair up).
+    rank = static_cast<int>(cg::this_cluster().block_rank());
+    cg::this_cluster().sync();
+  }
+  for (int k = rank + CS * warp; k < P.nchunks; k += CS * kTSWarps) {
     const int j0 = k * P.chunk, j1 = min(P.V, j0 + P.chunk);
     float s;
     if (cj.hi == 0.0f)
@@ -183,9 +201,18 @@ __device__ double residual_pass(const NodeRows<E>& R, const TreeSampleParams& P,
       s = filtered ? chunk_residual<E, true, false>(R, j0, j1, P.c, cj)
                    : chunk_residual<E, false, false>(R, j0, j1, P.c, cj);
     const double t = warp_sum_d(static_cast<double>(s));
-    if (lane == 0) sh.chunk_sum[k] = t;
+    if (lane == 0) {
+      if constexpr (CS > 1) {
+        cg::cluster_group cl = cg::this_cluster();
+#pragma unroll
+        for (int r = 0; r < CS; ++r) *cl.map_shared_rank(&sh.chunk_sum[k], r) = t;
+      } else {
+        sh.chunk_sum[k] = t;
+      }
+    }
   }
-  __syncthreads();
+  if constexpr (CS > 1) cg::this_cluster().sync();  // every block holds every chunk sum
+  else __syncthreads();
   if (warp == 0) {
     double t = 0.0;
     for (int k = lane; k < P.nchunks; k += 32) t += sh.chunk_sum[k];
@@ -253,26 +280,58 @@ __device__ int draw(const NodeRows<E>& R, const TreeSampleParams& P, Coef cj, do
   double before = sh.bcast_d;
   const bool rounding = before < 0.0;
   const int j0 = k * P.chunk, j1 = min(P.V, j0 + P.chunk);
-  for (int t0 = j0; t0 < j1; t0 += kTSThreads) {
-    const int j = t0 + static_cast<int>(threadIdx.x);
-    const float w = j < j1 ? resid(R, Elem<E>::load(R.lt + j), Elem<E>::load(R.ld + j), j, P.c, cj) : 0.0f;
-    double tile;
-    const double ex = block_exclusive_scan_d<kTSThreads>(static_cast<double>(w), sh.red, &tile);
-    if (w > 0.0f) {
-      if (!rounding && before + ex + w > target) atomicMin(&sh.hit, j);
-      atomicMax(&sh.last_pos, j);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // Tiles of 2 * kTSThreads ids, thread t holding ids 2t and 2t + 1 (ids
+  // ascend with the thread index): a warp scan of the pairs, one warp's
+  // scan of the warp totals, then the first id whose inclusive prefix
+  // exceeds u * total.
+  for (int t0 = j0; t0 < j1; t0 += 2 * kTSThreads) {
+    const int ja = t0 + 2 * static_cast<int>(threadIdx.x), jb = ja + 1;
+    const float wa = ja < j1 ? resid(R, Elem<E>::load(R.lt + ja), Elem<E>::load(R.ld + ja), ja, P.c, cj) : 0.0f;
+    const float wb = jb < j1 ? resid(R, Elem<E>::load(R.lt + jb), Elem<E>::load(R.ld + jb), jb, P.c, cj) : 0.0f;
+    const double mine = static_cast<double>(wa) + static_cast<double>(wb);
+    double incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const double y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) sh.red[warp] = incl;
+    if (wb > 0.0f) atomicMax(&sh.last_pos, jb);
+    else if (wa > 0.0f) atomicMax(&sh.last_pos, ja);
+    __syncthreads();
+    if (warp == 0) {
+      const double t = lane < kTSWarps ? sh.red[lane] : 0.0;
+      double c = t;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const double y = __shfl_up_sync(0xffffffffu, c, o);
+        if (lane >= o) c += y;
+      }
+      sh.warp_before[lane] = c - t;
+      if (lane == 31) sh.tile_total = c;
+    }
+    __syncthreads();
+    if (!rounding) {
+      const double ex = before + sh.warp_before[warp] + (incl - mine);  // before id ja
+      if (wa > 0.0f && ex + wa > target) atomicMin(&sh.hit, ja);
+      else if (wb > 0.0f && ex + static_cast<double>(wa) + wb > target) atomicMin(&sh.hit, jb);
     }
     __syncthreads();
     if (sh.hit != INT32_MAX) break;
-    before += tile;
+    before += sh.tile_total;
   }
   return sh.hit != INT32_MAX ? sh.hit : sh.last_pos;
 }
 
-template <typename E>
+template <typename E, int CS>
 __global__ void __launch_bounds__(kTSThreads) tree_sample_kernel(TreeSampleParams P) {
   __shared__ TSShared sh;
-  const int b = blockIdx.x;
+  const int b = blockIdx.x / CS;
+  // Only the first block of a tree's cluster writes the tree's outputs (the
+  // others hold the same values).
+  bool writer = true;
+  if constexpr (CS > 1) writer = cg::this_cluster().block_rank() == 0;
   const int N = P.N;
   const int64_t base = static_cast<int64_t>(b) * N;
   const int32_t* par = P.parents + base;
@@ -310,11 +369,11 @@ __global__ void __launch_bounds__(kTSThreads) tree_sample_kernel(TreeSampleParam
   int32_t* path = P.path + static_cast<int64_t>(b) * L;
   int32_t* out = P.out_tokens + static_cast<int64_t>(b) * L;
   if (status) {
-    for (int i = threadIdx.x; i < L; i += kTSThreads) {
+    for (int i = threadIdx.x; writer && i < L; i += kTSThreads) {
       path[i] = -1;
       out[i] = -1;
     }
-    if (threadIdx.x == 0) {
+    if (writer && threadIdx.x == 0) {
       P.accept_len[b] = 0;
       if (P.row_status) P.row_status[b] = static_cast<int32_t>(status);
     }
@@ -323,8 +382,32 @@ __global__ void __launch_bounds__(kTSThreads) tree_sample_kernel(TreeSampleParam
 
   const E* tgt = static_cast<const E*>(P.target);
   const E* dft = static_cast<const E*>(P.draft);
+  // Every node's accept test inputs, all loads in flight together: p(x) and
+  // q(x) from the parent rows' offsets and kept masses with the
+  // double-precision exp2, and the node's uniform.
+  for (int i = threadIdx.x; i < 3 * (N - 1); i += kTSThreads) {
+    const int n = 1 + i / 3, which = i - 3 * (n - 1);
+    double v = 0.0;
+    if (which == 2) {
+      v = static_cast<double>(P.u_accept[base + n]);
+    } else {
+      const int64_t prow = base + par[n];
+      const int x = tok[n];
+      const RowStats st = which == 0 ? P.ts[prow] : P.ds[prow];
+      RowDist r;
+      r.mc = st.mc;
+      r.invK = 0.0f;
+      r.tau = st.tau;
+      r.cut = st.cut;
+      if (sv_in(x, P.V))
+        v = exact_prob(r, which == 0 ? Elem<E>::load(tgt + prow * P.t_stride + x) : Elem<E>::load(dft + prow * P.d_stride + x),
+                       x, P.c, st.K);
+    }
+    sh.test[n][which] = v;
+  }
+  __syncthreads();
   int node = 0, d = 0;
-  if (threadIdx.x == 0) path[0] = 0;
+  if (writer && threadIdx.x == 0) path[0] = 0;
   // Every iteration either moves one level down (parents[n] < n and depths
   // <= D were checked above) or returns: at most D + 1 iterations.
   for (;;) {
@@ -349,31 +432,14 @@ __global__ void __launch_bounds__(kTSThreads) tree_sample_kernel(TreeSampleParam
     bool sums_for_cj = false;  // chunk sums of the current residual are in shared memory
     int next = -1;
     for (int ch = sh.first_child[node]; ch >= 0; ch = sh.next_sib[ch]) {
-      // The accept test in double: p(x) (thread 0) and q(x) (thread 1) from
-      // the rows' offsets and kept masses with the double-precision exp2.
-      if (threadIdx.x < 2) {
-        const int x = tok[ch];
-        double v = 0.0;
-        if (sv_in(x, P.V))
-          v = threadIdx.x == 0 ? exact_prob(R.p, Elem<E>::load(R.lt + x), x, P.c, P.ts[row].K)
-                               : exact_prob(R.q, Elem<E>::load(R.ld + x), x, P.c, P.ds[row].K);
-        sh.pq[threadIdx.x] = v;
-      }
-      __syncthreads();
-      if (threadIdx.x == 0) {
-        const double p = sh.pq[0], q = sh.pq[1];
-        const double u = P.u_accept[base + ch];
-        sh.bcast_i = u * q * W < fmax(0.0, p - cj * q);
-      }
-      __syncthreads();
-      const bool accept = sh.bcast_i != 0;
-      __syncthreads();
-      if (accept) {
+      const double p = sh.test[ch][0], q = sh.test[ch][1], u = sh.test[ch][2];
+      // Every thread evaluates the same test on the same values.
+      if (u * q * W < fmax(0.0, p - cj * q)) {
         next = ch;
         break;
       }
       const double c_new = cj + W;
-      const double W_new = residual_pass(R, P, split_coef(c_new), sh);
+      const double W_new = residual_pass<E, CS>(R, P, split_coef(c_new), sh);
       if (W_new > 0.0) {
         cj = c_new;
         W = W_new;
@@ -386,20 +452,20 @@ __global__ void __launch_bounds__(kTSThreads) tree_sample_kernel(TreeSampleParam
     if (next >= 0) {
       node = next;
       ++d;
-      if (threadIdx.x == 0 && sv_in(d, L)) {
+      if (writer && threadIdx.x == 0 && sv_in(d, L)) {
         path[d] = node;
         out[d - 1] = tok[node];
       }
       continue;
     }
-    double total = sums_for_cj ? W : residual_pass(R, P, split_coef(cj), sh);
+    double total = sums_for_cj ? W : residual_pass<E, CS>(R, P, split_coef(cj), sh);
     const int y = draw(R, P, split_coef(cj), total, P.u_final[b], sh);
-    if (threadIdx.x == 0) {
+    if (writer && threadIdx.x == 0) {
       out[d] = y;
       P.accept_len[b] = d;
       if (P.row_status) P.row_status[b] = static_cast<int32_t>(status);
     }
-    for (int i = d + 1 + threadIdx.x; i < L; i += kTSThreads) {
+    for (int i = d + 1 + threadIdx.x; writer && i < L; i += kTSThreads) {
       path[i] = -1;
       out[i] = -1;
     }
@@ -470,10 +536,38 @@ sv_status tree_sample(const sv_tree_sample_desc& d, const void* target, const vo
   P.path = path;
   P.out_tokens = out_tokens;
   P.row_status = row_status;
-  if (d.dtype == SV_BF16)
-    tree_sample_kernel<uint16_t><<<d.batch, kTSThreads, 0, stream>>>(P);
-  else
-    tree_sample_kernel<float><<<d.batch, kTSThreads, 0, stream>>>(P);
+  // A cluster of two blocks per tree while the trees leave SMs idle.
+  static std::atomic<int> sms[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+  int nsm = sms[dev].load(std::memory_order_relaxed);
+  if (nsm == 0) {
+    if (cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || nsm <= 0) nsm = 148;
+    sms[dev].store(nsm, std::memory_order_relaxed);
+  }
+  const bool pair = 2LL * d.batch <= nsm;
+  const bool bf = d.dtype == SV_BF16;
+  if (pair) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * d.batch));
+    cfg.blockDim = dim3(kTSThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = bf ? cudaLaunchKernelEx(&cfg, tree_sample_kernel<uint16_t, 2>, P)
+                             : cudaLaunchKernelEx(&cfg, tree_sample_kernel<float, 2>, P);
+    if (e != cudaSuccess) return SV_ERR_CUDA;
+  } else if (bf) {
+    tree_sample_kernel<uint16_t, 1><<<d.batch, kTSThreads, 0, stream>>>(P);
+  } else {
+    tree_sample_kernel<float, 1><<<d.batch, kTSThreads, 0, stream>>>(P);
+  }
   if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
   note_launch(stream);
   return SV_OK;

@@ -4,7 +4,9 @@ with many siblings on tiny vocabularies (long runs of rejections, repeated
 tokens), ragged and unaligned rows, vocabularies of more than 256 chunks,
 the zero-residual fallback, and invalid trees.
 
-The path, accept length and every emitted token must equal the oracle's.
+The path, accept length and every emitted token must equal the oracle's,
+whether a tree is walked by one thread block or by a cluster of two that
+splits every residual pass.
 A tree may differ only where one of the oracle's decisions on it lies
 within NEAR = 1e-6 of its threshold (in units of the uniform), the same
 margin as the chain verify.  The GPU takes each accept test in double (p(x)
@@ -110,6 +112,14 @@ def test_unaligned_rows_and_large_vocab(sv):
     cfg = synth.TreeConfig("t", 5, 6, 600_000, "f32", 3, 3, 2.0, 0.5, 4.0)
     tr = synth.make_tree_sample_inputs(cfg, seed=4, batch=2)
     _compare(_run(sv, tr, 1.0, 1.0, "f32"), _oracle(tr, 1.0, 1.0))
+
+
+def test_many_trees_one_block_each(sv):
+    """More trees than half the SMs: one thread block per tree instead of a
+    cluster of two (the smaller batches above take the clusters)."""
+    cfg = synth.TreeConfig("t", 9, 16, 3001, "bf16", 4, 4, 2.0, 0.6, 4.0)
+    tr = synth.make_tree_sample_inputs(cfg, seed=11, batch=200, draft_noise=1.5)
+    _compare(_run(sv, tr, 0.9, 0.9, "bf16"), _oracle(tr, 0.9, 0.9))
 
 
 def test_zero_residual_fallback(sv):
