@@ -283,7 +283,9 @@ size_t sv_tree_sample_workspace_size(const sv_tree_sample_desc* desc);
  *   row_status    optional [B] int32 (SV_ROW_*): invalid trees and trees with a
  *                 row of no finite logit emit nothing (accept_len 0, -1s).
  *
- * Launches: the row statistics of all 2*B*N rows, then one block per tree.
+ * Launches: the row statistics of all 2*B*N rows, then the walk: a cluster
+ * of two thread blocks per tree when 2*B does not exceed the SM count (the
+ * two split every residual pass), else one block per tree.
  */
 sv_status sv_verify_tree_sample(const sv_tree_sample_desc* desc, const void* target_logits,
                                 const void* draft_logits, const int32_t* parents, const int32_t* tokens,
