@@ -50,6 +50,7 @@ STATUS_BAD_TOKEN = 8       # tree: a node token outside [0, V)
 STATUS_EMPTY_ROW = 16      # a row whose logits are all -inf (no distribution)
 
 NEAR = 1e-6  # decisions closer than this to their threshold may legitimately differ
+ALTS = 3     # a top-p cut, and the one rank shorter and longer that NEAR admits
 
 
 # ---------------------------------------------------------------------------
@@ -79,7 +80,7 @@ def nucleus_order(logits: np.ndarray, tie_index: np.ndarray | None = None) -> np
     return np.lexsort((idx, -(logits + 0.0)))
 
 
-def top_p_filter(z: np.ndarray, top_p: float, order: np.ndarray):
+def top_p_filter(z: np.ndarray, top_p: float, order: np.ndarray, cut: dict | None = None):
     """[P3] §4.2 ``_apply_top_p`` on temperature-scaled logits ``z``.
 
     Steps as the page gives them: sort descending, softmax of the sorted
@@ -94,7 +95,12 @@ def top_p_filter(z: np.ndarray, top_p: float, order: np.ndarray):
 
     Returns (filtered z, boundary margin).  The margin is the distance of
     top_p from the nearest cumulative value that decides the cut; inf when
-    no filtering happens.
+    no filtering happens.  When ``cut`` is a dict it also receives (for
+    reporting only) "alts": the filtered z of every other cut whose
+    keep-or-drop comparison lies within NEAR of top_p -- one rank fewer when
+    the last kept rank's comparison is that close, one rank more when the
+    first removed rank's is -- so that a caller can take each decision under
+    every cut that rounding could produce.
     """
     z = np.asarray(z, dtype=np.float64)
     if top_p >= 1.0:
@@ -112,22 +118,38 @@ def top_p_filter(z: np.ndarray, top_p: float, order: np.ndarray):
         margin = min(margin, abs(cum[kept - 1] - top_p))   # first cum above top_p
     if kept >= 2:
         margin = min(margin, abs(cum[kept - 2] - top_p))   # last cum at or below
+    if cut is not None:
+        alt_kept = []
+        if kept < cum.size and abs(cum[kept - 1] - top_p) < NEAR:
+            alt_kept.append(kept + 1)   # the first removed rank kept as well
+        if kept >= 2 and abs(cum[kept - 2] - top_p) < NEAR:
+            alt_kept.append(kept - 1)   # the last kept rank removed
+        for n in alt_kept:
+            alt = z.copy()
+            alt[order[n:]] = -np.inf
+            cut["alts"].append(alt)
     return out, margin
 
 
 def dist(logits: np.ndarray, temperature: float, top_p: float,
-         tie_index: np.ndarray | None = None):
+         tie_index: np.ndarray | None = None, cut: dict | None = None):
     """Distribution of one position: softmax(top_p_filter(logits / T)).
 
     [P3] §4.2: ``logits / temperature`` -> ``_apply_top_p`` -> ``F.softmax``.
-    Returns (probabilities float64[V], top-p boundary margin).
+    Returns (probabilities float64[V], top-p boundary margin).  When ``cut``
+    is a dict it receives "alts": the distributions of the other cuts within
+    NEAR of top_p (see top_p_filter), empty when there are none.
     """
     logits = np.asarray(logits, dtype=np.float64)
     if not np.any(np.isfinite(logits)):
         raise ValueError("row has no finite logit")
     z = logits / float(temperature)
     order = nucleus_order(logits, tie_index) if top_p < 1.0 else None
-    filtered, margin = top_p_filter(z, top_p, order)
+    if cut is not None:
+        cut["alts"] = []
+    filtered, margin = top_p_filter(z, top_p, order, cut)
+    if cut is not None:
+        cut["alts"] = [softmax(a) for a in cut["alts"]]
     return softmax(filtered), margin
 
 
@@ -241,11 +263,23 @@ def verify_chain_row(target_logits: np.ndarray, draft_logits: np.ndarray | None,
     Returns dict(tokens [γ+1] int64 (-1 padded), k, p_draft [γ], q_draft [γ],
     margin (smallest decision margin on the path that produced the output),
     near_from (the first output position decided by a decision whose margin
-    is below NEAR -- the top-p cut of row i or the accept test of draft i
-    decide position i, the draw decides position k --; γ+1 when none),
-    pq_margin [γ+1, 2] (top-p margins of target row i and draft row i, for
-    every row whose distribution was computed; inf otherwise),
-    status, resample_fallback (bool: residual mass was 0)).
+    is below NEAR -- the accept test of draft i decides position i, the draw
+    decides position k --; γ+1 when none), pq_margin [γ+1, 2] (top-p margins
+    of target row i and draft row i, for every row whose distribution was
+    computed; inf otherwise), p_alts / q_alts [γ, ALTS] (p_i(d_i) and
+    q_i(d_i) under every admissible cut, the oracle's own first; NaN padded),
+    final_alts [ALTS^2] (every token the draw at k gives under the admissible
+    cuts of rows k, the oracle's own first; -1 padded), status,
+    resample_fallback (bool: residual mass was 0)).
+
+    Margins and alternatives (reporting only; no result depends on them).  A
+    top-p cut whose deciding cumulative sum lies within NEAR of top_p could
+    come out one rank shorter or longer under rounding (top_p_filter's
+    "alts"); every accept test and the draw are taken under each admissible
+    pair (target cut, draft cut) of their row.  An accept test whose outcome
+    differs between pairs has margin 0; otherwise its margin is the smallest
+    |u - p/q| over the pairs.  The draw's margin is the smallest over the
+    pairs, and the tokens it gives are listed in final_alts.
     """
     target_logits = np.asarray(target_logits, dtype=np.float64)
     gamma = target_logits.shape[0] - 1
@@ -254,7 +288,8 @@ def verify_chain_row(target_logits: np.ndarray, draft_logits: np.ndarray | None,
     tokens = np.full(gamma + 1, -1, dtype=np.int64)
     res = dict(tokens=tokens, k=0, p_draft=np.zeros(gamma), q_draft=np.zeros(gamma),
                margin=np.inf, near_from=gamma + 1, pq_margin=np.full((gamma + 1, 2), np.inf),
-               status=0, resample_fallback=False)
+               p_alts=np.full((gamma, ALTS), np.nan), q_alts=np.full((gamma, ALTS), np.nan),
+               final_alts=np.full(ALTS * ALTS, -1, np.int64), status=0, resample_fallback=False)
 
     if np.any((ids < 0) | (ids >= vocab)):
         res["status"] = STATUS_BAD_DRAFT_ID
@@ -281,63 +316,78 @@ def verify_chain_row(target_logits: np.ndarray, draft_logits: np.ndarray | None,
         return res
     margins = []   # margin of every decision on the output's path
     decides = []   # the output position each of those decisions decides
+    cands = {}     # (i, 0 target / 1 draft) -> [own distribution, admissible alternatives]
 
     def p_row(i):
-        p, mg = dist(target_logits[i], temperature, top_p)
-        margins.append(mg)
-        decides.append(i)
+        cut = {}
+        p, mg = dist(target_logits[i], temperature, top_p, cut=cut)
+        cands[(i, 0)] = [p] + cut["alts"]
         res["pq_margin"][i, 0] = mg
         return p
 
     def q_row(i):
+        cut = {}
         if d2t is None:
-            q, mg = dist(draft_logits[i], temperature, top_p)
+            q, mg = dist(draft_logits[i], temperature, top_p, cut=cut)
         else:
             scattered = d2t_scatter(draft_logits[i], d2t, vocab)[0]
-            q, mg = dist(scattered, temperature, top_p)
-        margins.append(mg)
-        decides.append(i)
+            q, mg = dist(scattered, temperature, top_p, cut=cut)
+        cands[(i, 1)] = [q] + cut["alts"]
         res["pq_margin"][i, 1] = mg
         return q
+
+    def record(i, x):
+        """p_i(x), q_i(x) under the row's own and admissible cuts."""
+        for key, col in (("p", 0), ("q", 1)):
+            vals = [d[x] for d in cands[(i, col)]]
+            res[key + "_draft"][i] = vals[0]
+            res[key + "_alts"][i, :len(vals)] = vals
 
     k = gamma
     p_k = q_k = None
     for i in range(gamma):
         p_i, q_i = p_row(i), q_row(i)
         x = ids[i]
-        res["p_draft"][i] = p_i[x]
-        res["q_draft"][i] = q_i[x]
+        record(i, x)
         accept = u_accept[i] * q_i[x] < p_i[x]
-        if q_i[x] > 0.0:
-            margins.append(abs(float(u_accept[i]) - p_i[x] / q_i[x]))
-            decides.append(i)
+        outcomes, mg = set(), np.inf
+        for p in cands[(i, 0)]:
+            for q in cands[(i, 1)]:
+                outcomes.add(bool(u_accept[i] * q[x] < p[x]))
+                if q[x] > 0.0:
+                    mg = min(mg, abs(float(u_accept[i]) - p[x] / q[x]))
+        margins.append(0.0 if len(outcomes) > 1 else mg)
+        decides.append(i)
         if not accept:
             k = i
             p_k, q_k = p_i, q_i
             break
+
+    def draw(p, q):
+        """(token, margin, fallback) of the draw at k under one pair of cuts."""
+        if q is None:                           # bonus token from p_γ, [P3] §3.1
+            return inverse_cdf(p, float(u_resample)) + (False,)
+        residual = np.maximum(0.0, p - q)       # norm(max(0, p - q)), [P3] §3.1
+        if residual.sum() > 0.0:
+            return inverse_cdf(residual, float(u_resample)) + (False,)
+        return inverse_cdf(p, float(u_resample)) + (True,)
+
     if k < gamma:
         # The remaining positions are still scored by the target ([P3] §4.2
         # computes every position before deciding); record p/q for them.
         for i in range(k + 1, gamma):
-            p_i, mg_p = dist(target_logits[i], temperature, top_p)
-            if d2t is None:
-                q_i, mg_q = dist(draft_logits[i], temperature, top_p)
-            else:
-                q_i, mg_q = dist(d2t_scatter(draft_logits[i], d2t, vocab)[0], temperature, top_p)
-            res["p_draft"][i] = p_i[ids[i]]
-            res["q_draft"][i] = q_i[ids[i]]
-            res["pq_margin"][i] = (mg_p, mg_q)
-        residual = np.maximum(0.0, p_k - q_k)   # norm(max(0, p - q)), [P3] §3.1
-        if residual.sum() > 0.0:
-            tok, mg = inverse_cdf(residual, float(u_resample))
-        else:
-            res["resample_fallback"] = True
-            tok, mg = inverse_cdf(p_k, float(u_resample))
+            p_row(i), q_row(i)
+            record(i, ids[i])
+        pairs = [(p, q) for p in cands[(k, 0)] for q in cands[(k, 1)]]
     else:
-        p_g = p_row(gamma)                      # bonus token from p_γ, [P3] §3.1
-        tok, mg = inverse_cdf(p_g, float(u_resample))
-    margins.append(mg)
+        p_row(gamma)
+        pairs = [(p, None) for p in cands[(gamma, 0)]]
+    finals = [draw(p, q) for p, q in pairs]
+    tok, _, res["resample_fallback"] = finals[0]
+    margins.append(min(f[1] for f in finals))
     decides.append(k)
+    alts = list(dict.fromkeys(f[0] for f in finals))
+    res["final_alts"][:len(alts)] = alts
     tokens[:k] = ids[:k]
     tokens[k] = tok
     res["k"] = k
@@ -362,7 +412,9 @@ def verify_chain(target_logits, draft_logits, draft_ids, u_accept, u_resample,
     out = dict(tokens=np.full((B, gp1), -1, np.int64), num_accepted=np.zeros(B, np.int64),
                p_draft=np.zeros((B, gamma)), q_draft=np.zeros((B, gamma)),
                margin=np.full(B, np.inf), near_from=np.full(B, gp1, np.int64),
-               pq_margin=np.full((B, gp1, 2), np.inf), status=np.zeros(B, np.int64),
+               pq_margin=np.full((B, gp1, 2), np.inf), p_alts=np.full((B, gamma, ALTS), np.nan),
+               q_alts=np.full((B, gamma, ALTS), np.nan), final_alts=np.full((B, ALTS * ALTS), -1, np.int64),
+               status=np.zeros(B, np.int64),
                resample_fallback=np.zeros(B, bool))
     for b in rows:
         r = verify_chain_row(
@@ -377,6 +429,9 @@ def verify_chain(target_logits, draft_logits, draft_ids, u_accept, u_resample,
         out["margin"][b] = r["margin"]
         out["near_from"][b] = r["near_from"]
         out["pq_margin"][b] = r["pq_margin"]
+        out["p_alts"][b] = r["p_alts"]
+        out["q_alts"][b] = r["q_alts"]
+        out["final_alts"][b] = r["final_alts"]
         out["status"][b] = r["status"]
         out["resample_fallback"][b] = r["resample_fallback"]
     return out
@@ -551,7 +606,18 @@ def verify_tree_sample_row(target_logits: np.ndarray, draft_logits: np.ndarray,
     the last token was drawn from.
 
     Returns dict(accept_len, path [max_depth+1], out_tokens [max_depth+1]
-    (-1 padded), status, margin, resample_fallback).
+    (-1 padded), status, margin, resample_fallback, final_alts [ALTS^2]
+    (every token the final draw gives under the admissible cuts, the
+    oracle's own first; -1 padded)).
+
+    Margins and alternatives (reporting only; no result depends on them), as
+    for the chain: a top-p cut within NEAR of top_p could come out one rank
+    shorter or longer (top_p_filter's "alts"), and each node's children are
+    tested under every admissible pair (target cut, draft cut) of the node.
+    When the pairs accept different children (or one accepts and another
+    none) the node's margin is 0; otherwise the margin is the smallest
+    |u - r(x)/q(x)| over the pairs' tests, and the final draw's the smallest
+    over the pairs, whose tokens are listed in final_alts.
     """
     target_logits = np.asarray(target_logits, dtype=np.float64)
     draft_logits = np.asarray(draft_logits, dtype=np.float64)
@@ -560,7 +626,7 @@ def verify_tree_sample_row(target_logits: np.ndarray, draft_logits: np.ndarray,
     N, V = target_logits.shape
     L = max_depth + 1
     res = dict(accept_len=0, path=np.full(L, -1, np.int64), out_tokens=np.full(L, -1, np.int64),
-               status=0, margin=np.inf, resample_fallback=False)
+               status=0, margin=np.inf, resample_fallback=False, final_alts=np.full(ALTS * ALTS, -1, np.int64))
     status, _ = _tree_checks(parents, tokens, V, max_depth)
     if not (np.all(np.any(np.isfinite(target_logits), axis=1))
             and np.all(np.any(np.isfinite(draft_logits), axis=1))):
@@ -568,14 +634,12 @@ def verify_tree_sample_row(target_logits: np.ndarray, draft_logits: np.ndarray,
     if status:
         res["status"] = status
         return res
-    margins = []
-    node, chain = 0, [0]
-    while True:
-        p, mg_p = dist(target_logits[node], temperature, top_p)
-        q, mg_q = dist(draft_logits[node], temperature, top_p)
-        margins += [mg_p, mg_q]
+
+    def children_pass(node, p, q, log):
+        """Test node's children against r = p under one pair of cuts.
+        Returns (accepted child or None, final r, margins, fallback)."""
         r = p.copy()
-        nxt = None
+        mgs, fallback = [], False
         for c in range(node + 1, N):
             if parents[c] != node:
                 continue
@@ -584,26 +648,44 @@ def verify_tree_sample_row(target_logits: np.ndarray, draft_logits: np.ndarray,
             accept = u * q[x] < r[x]
             if q[x] > 0.0:
                 threshold = min(1.0, r[x] / q[x])
-                margins.append(abs(u - r[x] / q[x]))
+                mgs.append(abs(u - r[x] / q[x]))
             else:
                 threshold = 1.0 if r[x] > 0.0 else 0.0
-            if trace is not None:
-                trace.append(dict(node=c, token=int(x), threshold=threshold, accepted=bool(accept)))
+            if log is not None:
+                log.append(dict(node=c, token=int(x), threshold=threshold, accepted=bool(accept)))
             if accept:
-                nxt = c
-                break
+                return c, r, mgs, fallback
             residual = np.maximum(0.0, r - q)
             if residual.sum() > 0.0:
                 r = residual / residual.sum()
             else:
-                res["resample_fallback"] = True
+                fallback = True
+        return None, r, mgs, fallback
+
+    margins = []
+    node, chain = 0, [0]
+    while True:
+        cut_p, cut_q = {}, {}
+        p, _ = dist(target_logits[node], temperature, top_p, cut=cut_p)
+        q, _ = dist(draft_logits[node], temperature, top_p, cut=cut_q)
+        passes = [children_pass(node, pp, qq, trace if (pp is p and qq is q) else None)
+                  for pp in [p] + cut_p["alts"] for qq in [q] + cut_q["alts"]]
+        nxt, r, _, fallback = passes[0]
+        res["resample_fallback"] |= fallback
+        for other in passes:
+            margins += other[2]
+        if any(other[0] != nxt for other in passes):
+            margins.append(0.0)            # the accepted child depends on the cut
         if nxt is None:
             break
         node = nxt
         chain.append(node)
     # r is p when the node has no children, else the residual after the last rejection.
-    tok, mg = inverse_cdf(r, float(u_final))
-    margins.append(mg)
+    draws = [inverse_cdf(other[1], float(u_final)) for other in passes]
+    tok = draws[0][0]
+    margins.append(min(mg for _, mg in draws))
+    alts = list(dict.fromkeys(t for t, _ in draws))
+    res["final_alts"][:len(alts)] = alts
     if trace is not None:
         trace.append(dict(final=True, weights=r / r.sum()))
     d = len(chain) - 1
@@ -624,12 +706,13 @@ def verify_tree_sample(target_logits, draft_logits, parents, tokens, u_accept, u
     L = max_depth + 1
     out = dict(accept_len=np.zeros(B, np.int64), path=np.full((B, L), -1, np.int64),
                out_tokens=np.full((B, L), -1, np.int64), status=np.zeros(B, np.int64),
-               margin=np.full(B, np.inf), resample_fallback=np.zeros(B, bool))
+               margin=np.full(B, np.inf), resample_fallback=np.zeros(B, bool),
+               final_alts=np.full((B, ALTS * ALTS), -1, np.int64))
     for b in (range(B) if rows is None else rows):
         r = verify_tree_sample_row(target_logits[b], np.asarray(draft_logits)[b], np.asarray(parents)[b],
                                    np.asarray(tokens)[b], np.asarray(u_accept)[b],
                                    float(np.asarray(u_final)[b]), temperature, top_p, max_depth)
-        for k in ("accept_len", "path", "out_tokens", "status", "margin", "resample_fallback"):
+        for k in ("accept_len", "path", "out_tokens", "status", "margin", "resample_fallback", "final_alts"):
             out[k][b] = r[k]
     return out
 

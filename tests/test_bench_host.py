@@ -76,12 +76,12 @@ def test_parity_sample_counts_mismatches(name):
     base = bench.cpu_baseline(cfg_b, inputs, 0.0, sink=sampled, cores=2)
     assert base["kind"] == "oracle" and base["cores"] == 2 and len(sampled) >= 1
     # the workers' rows are the oracle's own rows
-    rows = [b for b, _, _ in sampled]
+    rows = [b for b, _, _, _ in sampled]
     direct = bench.oracle_rows(cfg_b, host, rows)
-    for b, tok, margin in sampled:
+    for b, tok, margin, others in sampled:
         assert np.array_equal(tok, direct[key][b])
     got = np.full((4, sampled[0][1].size), -1, np.int64)
-    for b, tok, _ in sampled:
+    for b, tok, _, _ in sampled:
         got[b] = tok
     assert bench.parity_sample(cfg_b, sampled, got) == {"rows": len(sampled), "mismatch": 0,
                                                         "near_threshold": 0}

@@ -90,12 +90,13 @@ def test_qwen3_d2t_full_size(sv, qwen3):
 
 def test_qwen3_d2t_every_batch_row(sv, qwen3):
     """All 256 batch rows of the full workload against the oracle, which runs
-    one batch row per task on every host core: tokens and accept counts must
-    match, except in rows with an oracle decision within 1e-6 of its
-    threshold.  On 151936-id rows one logit near the top-p cut carries about
-    1e-6 to 1e-8 of the mass, so every row's cut is that close to top_p and
-    every row counts as near; the mismatches among them must stay rare (at
-    most 2% of the rows)."""
+    one batch row per task on every host core.  On 151936-id rows nearly
+    every top-p cut lies within 1e-6 of top_p (one logit there carries 1e-6
+    to 1e-8 of the mass), so the oracle takes each decision under every cut
+    that close: tokens and accept counts must equal one of the token rows it
+    admits, except in rows with a decision within 1e-6 of its threshold under
+    one of those cuts.  Such rows must stay a small minority, and mismatches
+    among them rare (at most 2% of the rows)."""
     import bench
     x, ids = qwen3
     got = run_chain(sv, x, ids)
@@ -106,16 +107,20 @@ def test_qwen3_d2t_every_batch_row(sv, qwen3):
         done, _ = pool.rows(range(x["batch"]))
     finally:
         pool.close()
-    assert sorted(b for b, _, _ in done) == list(range(x["batch"]))
-    near = near_mis = 0
-    for b, want, margin in done:
-        same = np.array_equal(got["tokens"][b].astype(np.int64), want)
+    assert sorted(r[0] for r in done) == list(range(x["batch"]))
+    near = near_mis = multi = 0
+    for b, want, margin, others in done:
+        tok = got["tokens"][b].astype(np.int64)
+        same = any(np.array_equal(tok, w) for w in [want] + others)
+        multi += int(bool(others))
         if margin < O.NEAR:
             near += 1
             near_mis += int(not same)
         else:
-            assert same, (b, got["tokens"][b], want, margin)
-    print(f"[qwen3 d2t, all {len(done)} batch rows] near-threshold={near} near-threshold mismatches={near_mis}")
+            assert same, (b, got["tokens"][b], want, others, margin)
+    print(f"[qwen3 d2t, all {len(done)} batch rows] near-threshold={near} near-threshold mismatches={near_mis} "
+          f"rows with more than one admissible draw={multi}")
+    assert near <= len(done) // 5, near
     assert near_mis <= len(done) // 50, near_mis
 
 

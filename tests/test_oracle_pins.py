@@ -319,3 +319,92 @@ def test_top_k_equals_repeated_selection(seed):
         want.append(best)
         left.remove(best)
     assert O.top_k(x, k).tolist() == want
+
+
+# ---------------------------------------------------------------------------
+# Top-p cuts within NEAR of top_p (reporting only: no result depends on it):
+# the alternative cuts one rank shorter or longer, and chain decisions taken
+# under every admissible pair of cuts, on rows whose cumulative masses are
+# known in closed form: cum = 0.5, 0.8, 0.95, 1.0.
+
+PROBS = [0.5, 0.3, 0.15, 0.05]
+
+
+def _row_of(probs):
+    return np.log(np.asarray(probs, dtype=np.float64))
+
+
+def test_cut_alternative_one_rank_shorter():
+    # top_p just above 0.8: rank 2 is kept because cum[1] = 0.8 <= top_p, a
+    # comparison 1e-9 from flipping; the alternative keeps ranks 0 and 1.
+    cut = {}
+    p, mg = O.dist(_row_of(PROBS), 1.0, 0.8 + 1e-9, cut=cut)
+    assert p[3] == 0.0 and p[2] > 0.0 and mg < 1e-8
+    assert len(cut["alts"]) == 1
+    np.testing.assert_allclose(cut["alts"][0], [0.625, 0.375, 0.0, 0.0], rtol=1e-12)
+
+
+def test_cut_alternative_one_rank_longer():
+    # top_p just below 0.95: rank 3 is removed because cum[2] = 0.95 > top_p;
+    # the alternative keeps every id.
+    cut = {}
+    p, mg = O.dist(_row_of(PROBS), 1.0, 0.95 - 1e-9, cut=cut)
+    assert p[3] == 0.0 and p[2] > 0.0
+    assert len(cut["alts"]) == 1
+    np.testing.assert_allclose(cut["alts"][0], PROBS, rtol=1e-12)
+
+
+def test_cut_far_from_top_p_has_no_alternative():
+    for top_p in (0.9, 1.0):
+        cut = {}
+        O.dist(_row_of(PROBS), 1.0, top_p, cut=cut)
+        assert cut["alts"] == []
+
+
+def test_chain_decisions_under_admissible_cuts():
+    """A one-draft chain whose target and draft rows all have a cut 1e-9 from
+    top_p = 0.8 (id 2 kept, or not)."""
+    t = np.stack([_row_of(PROBS)] * 2)
+    d = _row_of(PROBS)[None, :]
+    top_p = 0.8 + 1e-9
+    # Draft id 2: p = q = 0.15/0.95 accepts, but with the target's shorter
+    # cut p(2) = 0 rejects: the outcome depends on the cut, margin 0.
+    r = O.verify_chain_row(t, d, np.array([2]), np.array([0.25]), 0.5, 1.0, top_p)
+    assert r["margin"] == 0.0 and r["near_from"] == 0
+    np.testing.assert_allclose(r["p_alts"][0, :2], [0.15 / 0.95, 0.0], rtol=1e-12)
+    np.testing.assert_allclose(r["q_alts"][0, :2], [0.15 / 0.95, 0.0], rtol=1e-12)
+    assert np.isnan(r["p_alts"][0, 2])
+    # Draft id 0: p, q in {0.5/0.95, 0.625}, so p/q is 1, 0.5/0.95/0.625 or
+    # its inverse: accepted under every pair, margin 0.5/0.95/0.625 - 0.25.
+    # The bonus draw from p_1 with u = 0.3 gives id 0 under both cuts, with
+    # margins 0.5/0.95 - 0.3 and 0.625 - 0.3.
+    r = O.verify_chain_row(t, d, np.array([0]), np.array([0.25]), 0.3, 1.0, top_p)
+    assert r["k"] == 1 and r["tokens"].tolist() == [0, 0] and r["near_from"] == 2
+    assert r["final_alts"].tolist() == [0] + [-1] * 8
+    assert r["margin"] == pytest.approx(min(0.5 / 0.95 / 0.625 - 0.25, 0.5 / 0.95 - 0.3), rel=1e-12)
+    # u = 0.55 for the bonus draw: id 1 under the oracle's own cut (its CDF
+    # interval is [0.5/0.95, 0.8/0.95]), id 0 under the shorter one ([0, 0.625]).
+    r = O.verify_chain_row(t, d, np.array([0]), np.array([0.25]), 0.55, 1.0, top_p)
+    assert r["tokens"].tolist() == [0, 1]
+    assert r["final_alts"].tolist() == [1, 0] + [-1] * 7
+    assert r["margin"] == pytest.approx(0.55 - 0.5 / 0.95, rel=1e-12)
+    assert r["near_from"] == 2
+
+
+def test_chain_residual_draw_under_admissible_cuts():
+    """Rejection at 0 with q concentrated on the draft id: the residual
+    max(0, p - q) under each pair of cuts, closed form.  Target cut 1e-9 from
+    0.8 (p = (0.5, 0.3, 0.15, 0)/0.95, or (0.625, 0.375, 0, 0)); draft row
+    (0.97, 0.01, 0.01, 0.01) with top_p 0.8 keeps id 0 only."""
+    t = np.stack([_row_of(PROBS)] * 2)
+    d = _row_of([0.97, 0.01, 0.01, 0.01])[None, :]
+    top_p = 0.8 + 1e-9
+    # q = (1, 0, 0, 0): p/q = 0.5/0.95 or 0.625 at id 0; u = 0.9 rejects both.
+    # Residual (0, 0.3, 0.15, 0)/0.95 -> ids 1, 2 with weights 2/3, 1/3; or
+    # (0, 0.375, 0, 0) -> id 1 alone.  u = 0.7 draws id 2 from the first
+    # (margin 0.7 - 2/3), id 1 from the second (margin 0.3).
+    r = O.verify_chain_row(t, d, np.array([0]), np.array([0.9]), 0.7, 1.0, top_p)
+    assert r["k"] == 0 and r["tokens"].tolist() == [2, -1]
+    assert r["final_alts"].tolist() == [2, 1] + [-1] * 7
+    assert r["margin"] == pytest.approx(min(0.9 - 0.625, 0.7 - 2 / 3), rel=1e-12)
+    assert not r["resample_fallback"]

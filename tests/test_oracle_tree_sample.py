@@ -211,3 +211,28 @@ def test_invalid_trees_emit_nothing():
     bad[2] = -np.inf
     r = O.verify_tree_sample_row(t, bad, np.array([-1, 0, 0, 1]), np.array([0, 1, 2, 3]), u, 0.5, 1.0, 1.0, 3)
     assert r["status"] & O.STATUS_EMPTY_ROW
+
+
+def test_decisions_under_admissible_cuts():
+    """Rows (0.5, 0.3, 0.15, 0.05) with top_p 1e-9 above cum[1] = 0.8: id 2 is
+    kept, or not (the one-rank-shorter cut, (0.625, 0.375, 0, 0))."""
+    row = np.log(np.array([0.5, 0.3, 0.15, 0.05]))
+    top_p = 0.8 + 1e-9
+    rows = np.stack([row, row])
+    # Root with one child of token 2, u = 0.25: accepted under the oracle's own
+    # cuts (r = p, q(2) = p(2)), rejected once the target's cut drops id 2.
+    r = O.verify_tree_sample_row(rows, rows, np.array([-1, 0]), np.array([0, 2]), np.array([0.0, 0.25]),
+                                 0.3, 1.0, top_p, 1)
+    assert r["accept_len"] == 1 and r["margin"] == 0.0
+    # A root alone: the bonus draw from p with u = 0.55 gives id 1 under the
+    # own cut (CDF interval [0.5/0.95, 0.8/0.95]) and id 0 under the shorter
+    # one ([0, 0.625]); margin the smaller distance to an interval edge.
+    r = O.verify_tree_sample_row(rows[:1], rows[:1], np.array([-1]), np.array([0]), np.array([0.0]),
+                                 0.55, 1.0, top_p, 1)
+    assert r["out_tokens"].tolist() == [1, -1]
+    assert r["final_alts"].tolist() == [1, 0] + [-1] * 7
+    assert r["margin"] == pytest.approx(0.55 - 0.5 / 0.95, rel=1e-12)
+    # Far from any cut: one admissible token, the oracle's own.
+    r = O.verify_tree_sample_row(rows[:1], rows[:1], np.array([-1]), np.array([0]), np.array([0.0]),
+                                 0.55, 1.0, 0.9, 1)
+    assert r["final_alts"].tolist() == [int(r["out_tokens"][0])] + [-1] * 8
