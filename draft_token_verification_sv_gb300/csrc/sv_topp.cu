@@ -522,8 +522,9 @@ __device__ __forceinline__ int collect_ids(ToppShared& sh, const E* row, int len
 
 // Ids of the logits of the cut bin into this warp's region of sh.cand.j,
 // found by the slices' code bytes instead of their values: in slice q the
-// logits of the cut bin are those whose code equals tq[q] (>= 0; -1: the
-// slice has none; every slice's cut bin lies above its lowest bin).  Sixteen
+// logits of the cut bin are those of bin slot tq[q] (>= 0; -1: the slice has
+// none; every slice's cut bin lies above its lowest bin), whose code byte is
+// tq[q] + 1.  Sixteen
 // codes per 16-byte load, four compared at once (a byte of w ^ t is zero
 // exactly where the code matches); the scalar head and tail logits are
 // compared by value.  The codes are dropped from L2 afterwards (they are
@@ -558,7 +559,7 @@ __device__ __forceinline__ int collect_codes(ToppShared& sh, const uint8_t* code
     int cnt = 0;
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      const uint32_t t4 = t[u] >= 0 ? static_cast<uint32_t>(t[u]) * 0x01010101u : 0u;
+      const uint32_t t4 = t[u] >= 0 ? static_cast<uint32_t>(t[u] + 1) * 0x01010101u : 0u;  // code (t+1) mod 256
       const uint32_t w[4] = {cv[u].x, cv[u].y, cv[u].z, cv[u].w};
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
@@ -807,8 +808,9 @@ __device__ void resolve_candidates(ToppShared& sh, const RowSet& S, float c, flo
 }
 
 // Bin every logit of this thread's vectors with add (which returns the
-// logit's bin) and store the bins as bytes in logit order: vector k of
-// thread tid holds logits (k * kSThreads + tid) * EPV + 0..EPV-1 of the slice.
+// logit's code, (bin slot + 1) mod 256) and store the codes as bytes in
+// logit order: vector k of thread tid holds logits
+// (k * kSThreads + tid) * EPV + 0..EPV-1 of the slice.
 template <typename E, int VPT, typename F>
 __device__ __forceinline__ void bin_vectors(const uint4 (&raw)[VPT], uint8_t* codes, F&& add) {
   constexpr int EPV = Elem<E>::kPerVec;
@@ -827,6 +829,98 @@ __device__ __forceinline__ void bin_vectors(const uint4 (&raw)[VPT], uint8_t* co
       stg_hint(reinterpret_cast<uint32_t*>(codes) + k * kSThreads + tid, w[0], keep);
     } else {
       stg_hint(reinterpret_cast<uint2*>(codes) + k * kSThreads + tid, make_uint2(w[0], w[1]), keep);
+    }
+  }
+}
+
+// Binning of two logits at once with the packed FP32 instructions of sm_100
+// and later (two lanes per instruction), for the fast path of the slice
+// pass; bit for bit the scalar binning.  With y = l * c8 and fy = floor(y):
+// E = (2^23 + 1 + Gs) + (-y) rounded up is 2^23 + 1 + (Gs - fy) exactly (the
+// sum lies in [2^23, 2^24), where the spacing is 1, for every logit of the
+// slice), so the mantissa of E holds 1 + Gs - fy; clamped as an integer at
+// 1 + 255 it gives the bin idx = min(Gs - fy, 255) + 1 and the clamped floor
+// fy_c.  Then -(fy_c + 1)/8 = (E_c - 2^23 - 2 - Gs)/8 (exact), t = l*c plus
+// that in one rounding, and v = round(2^F * 2^t) by the magic addition.
+// The low byte of E_c is the logit's code, (idx + 1) mod 256.
+struct PairBins {
+  uint64_t nc8;    // (-c8, -c8)
+  uint64_t mg;     // (2^23 + 1 + Gs, ...)
+  uint64_t kg;     // (-(2^23 + 2 + Gs) / 8, ...)
+  uint64_t c;      // (c, c)
+  uint64_t fix;    // (2^F, 2^F)
+};
+constexpr uint32_t kPairBitsIdx0 = 0x4B000001u;  // bits of E_c for idx = 0
+
+__device__ __forceinline__ uint64_t pair_of(float a, float b) {
+  return static_cast<uint64_t>(__float_as_uint(a)) | (static_cast<uint64_t>(__float_as_uint(b)) << 32);
+}
+
+// (E_c bits, v) of the logits x = (x0, x1) packed low/high.
+__device__ __forceinline__ void bin_pair(uint64_t x, const PairBins& k, uint32_t& e0, uint32_t& e1, uint32_t& v0,
+                                         uint32_t& v1) {
+  uint64_t e;
+  asm("{\n\t.reg .b64 y;\n\t"
+      "mul.rn.f32x2 y, %1, %2;\n\t"
+      "add.rp.f32x2 %0, y, %3;\n\t"
+      "}"
+      : "=l"(e)
+      : "l"(x), "l"(k.nc8), "l"(k.mg));
+  e0 = min(static_cast<uint32_t>(e), kPairBitsIdx0 + 255u);
+  e1 = min(static_cast<uint32_t>(e >> 32), kPairBitsIdx0 + 255u);
+  const uint64_t ec = static_cast<uint64_t>(e0) | (static_cast<uint64_t>(e1) << 32);
+  uint64_t t;
+  asm("{\n\t.reg .b64 g;\n\t"
+      "fma.rn.f32x2 g, %1, %5, %2;\n\t"
+      "fma.rn.f32x2 %0, %3, %4, g;\n\t"
+      "}"
+      : "=l"(t)
+      : "l"(ec), "l"(k.kg), "l"(x), "l"(k.c), "l"(0x3E0000003E000000ull));  // (1/8, 1/8)
+  const float p0 = ex2(__uint_as_float(static_cast<uint32_t>(t)));
+  const float p1 = ex2(__uint_as_float(static_cast<uint32_t>(t >> 32)));
+  uint64_t w;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(w) : "l"(pair_of(p0, p1)), "l"(k.fix), "l"(0x4B0000004B000000ull));
+  v0 = static_cast<uint32_t>(w) - kMagicRoundBits;
+  v1 = static_cast<uint32_t>(w >> 32) - kMagicRoundBits;
+}
+
+// The slice's vectors through bin_pair: bin sums by shared-memory integer
+// reductions at whs_adj + 4 * E_c (whs_adj = the warp histogram's address
+// less 4 * kPairBitsIdx0), and the codes as bytes in logit order, as
+// bin_vectors stores them.
+template <typename E, int VPT>
+__device__ __forceinline__ void bin_vectors_x2(const uint4 (&raw)[VPT], uint8_t* codes, const PairBins& k,
+                                               uint32_t whs_adj) {
+  constexpr int EPV = Elem<E>::kPerVec;
+  const int tid = threadIdx.x;
+  const uint64_t keep = l2_policy_evict_last();
+#pragma unroll
+  for (int q = 0; q < VPT; ++q) {
+    const uint32_t wd[4] = {raw[q].x, raw[q].y, raw[q].z, raw[q].w};
+    uint32_t word[EPV / 4];
+#pragma unroll
+    for (int h = 0; h < EPV / 4; ++h) {
+      uint32_t eb[4];
+#pragma unroll
+      for (int pr = 0; pr < 2; ++pr) {
+        uint64_t x;
+        if constexpr (EPV == 4) {
+          x = static_cast<uint64_t>(wd[2 * pr]) | (static_cast<uint64_t>(wd[2 * pr + 1]) << 32);
+        } else {
+          const uint32_t w2 = wd[2 * h + pr];
+          x = static_cast<uint64_t>(w2 << 16) | (static_cast<uint64_t>(w2 & 0xffff0000u) << 32);
+        }
+        uint32_t v0, v1;
+        bin_pair(x, k, eb[2 * pr], eb[2 * pr + 1], v0, v1);
+        asm volatile("red.shared.add.u32 [%0], %1;" ::"r"(whs_adj + (eb[2 * pr] << 2)), "r"(v0) : "memory");
+        asm volatile("red.shared.add.u32 [%0], %1;" ::"r"(whs_adj + (eb[2 * pr + 1] << 2)), "r"(v1) : "memory");
+      }
+      word[h] = __byte_perm(__byte_perm(eb[0], eb[1], 0x0040), __byte_perm(eb[2], eb[3], 0x0040), 0x5410);
+    }
+    if constexpr (EPV == 4) {
+      stg_hint(reinterpret_cast<uint32_t*>(codes) + q * kSThreads + tid, word[0], keep);
+    } else {
+      stg_hint(reinterpret_cast<uint2*>(codes) + q * kSThreads + tid, make_uint2(word[0], word[1]), keep);
     }
   }
 }
@@ -891,10 +985,13 @@ __global__ void __launch_bounds__(kSThreads, 5) topp_slice_kernel(StatsLaunch L)
     }
     lm = fmaxf(lm, fmaxf(__low2float(m2), __high2float(m2)));
   } else {
+    // Three-input maxima (sm_100 and later), two logits per instruction.
 #pragma unroll
     for (int k = 0; k < VPT; ++k)
 #pragma unroll
-      for (int i = 0; i < EPV; ++i) lm = fmaxf(lm, Elem<E>::at(raw[k], i));
+      for (int i = 0; i < EPV; i += 2) {
+        asm("max.f32 %0, %0, %1, %2;" : "+f"(lm) : "f"(Elem<E>::at(raw[k], i)), "f"(Elem<E>::at(raw[k], i + 1)));
+      }
   }
   const float ms = block_max<kSThreads>(lm, sh.red_f);
 
@@ -926,7 +1023,15 @@ __global__ void __launch_bounds__(kSThreads, 5) topp_slice_kernel(StatsLaunch L)
       asm volatile("red.shared.add.u32 [%0], %1;" ::"r"(whs + idx * 4u), "r"(v) : "memory");
       return idx;
     };
-    bin_vectors<E, VPT>(raw, codes, add);
+    PairBins pk;
+    pk.nc8 = pair_of(-c8, -c8);
+    const float mg = kMagicRound + 1.0f + Gsf;  // exact: |Gs| < 2^22
+    pk.mg = pair_of(mg, mg);
+    const float kg = -(kMagicRound + 2.0f + Gsf) * 0.125f;
+    pk.kg = pair_of(kg, kg);
+    pk.c = pair_of(c, c);
+    pk.fix = pair_of(SliceShape<E>::kFix, SliceShape<E>::kFix);
+    bin_vectors_x2<E, VPT>(raw, codes, pk, whs - (kPairBitsIdx0 << 2));
     if (xv > -CUDART_INF_F) add(xv);
   } else if (live) {
     // Logits too large for the magic additions: the same bins by floorf and
@@ -937,7 +1042,7 @@ __global__ void __launch_bounds__(kSThreads, 5) topp_slice_kernel(StatsLaunch L)
       const unsigned v = __float2uint_rn(ex2(t) * SliceShape<E>::kFix);
       const int idx = static_cast<int>(Gsf - fy);
       if (v) atomicAdd(&wh[idx], v);
-      return static_cast<uint32_t>(idx);
+      return static_cast<uint32_t>(idx + 1) & 0xffu;  // the code
     };
     bin_vectors<E, VPT>(raw, codes, add);
     if (xv > -CUDART_INF_F) add(xv);
