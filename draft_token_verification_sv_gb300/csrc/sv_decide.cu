@@ -424,12 +424,17 @@ __global__ void __launch_bounds__(kDThreads, COMPACT ? (NC >= 8 ? 3 : 5) : (NC >
     for (int w = 0; w < kDWarps; ++w) l2 = max(l2, sh.red_i[w]);
     slast[seg] = l2;
   }
-  __threadfence();
+  // One fence on each side, by the thread that counts the block (the
+  // barriers order the other threads' writes and reads around it).
   __syncthreads();
-  if (tid == 0) sh.last = atomicAdd(P.counters + b, 1u) == static_cast<unsigned>(nseg - 1);
+  if (tid == 0) {
+    __threadfence();
+    const bool last = atomicAdd(P.counters + b, 1u) == static_cast<unsigned>(nseg - 1);
+    if (last) __threadfence();
+    sh.last = last;
+  }
   __syncthreads();
   if (!sh.last) return;
-  __threadfence();
 
   // The row's last block: the total, and the chunk that holds u * total.
   const float u = P.u_resample ? P.u_resample[b] : 0.0f;

@@ -545,18 +545,33 @@ __device__ __forceinline__ int collect_codes(ToppShared& sh, const uint8_t* code
   const uint4* c4 = reinterpret_cast<const uint4*>(codes);
   const int total = ns * Q16;
   int wn = 0;
+  uint4 na[U];
+  int nt[U];
+  auto load = [&](int g0) {
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int g = g0 + u * kSThreads + tid;
+      nt[u] = g < total ? tq[g >> kQShift] : -1;
+      na[u] = nt[u] >= 0 ? __ldcg(c4 + g) : make_uint4(0u, 0u, 0u, 0u);
+    }
+  };
+  load(0);
   for (int g0 = 0; g0 < total; g0 += U * kSThreads) {
     uint4 cv[U];
     int t[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      const int g = g0 + u * kSThreads + tid;
-      t[u] = g < total ? tq[g >> kQShift] : -1;
-      cv[u] = t[u] >= 0 ? __ldcg(c4 + g) : make_uint4(0u, 0u, 0u, 0u);
+      cv[u] = na[u];
+      t[u] = nt[u];
     }
-    // Zero-byte masks of w ^ t: the top bit of each matching byte.
-    uint32_t mk[U][4];
-    int cnt = 0;
+    if (g0 + U * kSThreads < total) load(g0 + U * kSThreads);
+    // Zero-byte masks of w ^ t (the top bit of each matching byte), folded
+    // into one bit per code of the batch: bit 16u + k for code k of vector u.
+    // (m >> 7) holds the four match bits at bits 0, 8, 16, 24; the product
+    // with 1 + 2^7 + 2^14 + 2^21 gathers them, without carries, at bits
+    // 21..24.
+    static_assert(U * 16 <= 32, "one bit per code of a batch");
+    uint32_t bm = 0u;
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const uint32_t t4 = t[u] >= 0 ? static_cast<uint32_t>(t[u] + 1) * 0x01010101u : 0u;  // code (t+1) mod 256
@@ -564,10 +579,11 @@ __device__ __forceinline__ int collect_codes(ToppShared& sh, const uint8_t* code
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const uint32_t x4 = w[i] ^ t4;
-        mk[u][i] = t[u] >= 0 ? ~(((x4 & 0x7f7f7f7fu) + 0x7f7f7f7fu) | x4 | 0x7f7f7f7fu) : 0u;
-        cnt += __popc(mk[u][i]);
+        const uint32_t mk = t[u] >= 0 ? ~(((x4 & 0x7f7f7f7fu) + 0x7f7f7f7fu) | x4 | 0x7f7f7f7fu) : 0u;
+        bm |= ((((mk >> 7) * 0x00204081u) >> 21) & 0xfu) << (16 * u + 4 * i);
       }
     }
+    const int cnt = __popc(bm);
     int incl = cnt;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -575,23 +591,15 @@ __device__ __forceinline__ int collect_codes(ToppShared& sh, const uint8_t* code
       if (lane >= o) incl += y;
     }
     int slot = wn + incl - cnt;
-    if (cnt) {
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int g = g0 + u * kSThreads + tid;
-        const int q = g >> kQShift;
-        const int off = (g & (Q16 - 1)) * 16;  // first code of the vector within slice q
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          uint32_t m = mk[u][i];
-          while (m) {
-            const int bit = __ffs(m) - 1;
-            m &= m - 1;
-            if (slot < kRegion) region[slot] = rs.head + q * SL + off + 4 * i + (bit >> 3);
-            ++slot;
-          }
-        }
-      }
+    // One loop over the set bits (its trip count is the lane's count, not
+    // one loop per word).
+    while (bm) {
+      const int k = __ffs(bm) - 1;
+      bm &= bm - 1;
+      const int g = g0 + (k >> 4) * kSThreads + tid;
+      const int q = g >> kQShift;
+      if (slot < kRegion) region[slot] = rs.head + q * SL + (g & (Q16 - 1)) * 16 + (k & 15);
+      ++slot;
     }
     wn += __shfl_sync(0xffffffffu, incl, 31);
   }
@@ -623,24 +631,18 @@ __device__ __forceinline__ int collect_codes(ToppShared& sh, const uint8_t* code
 // masses v = round(2^19 * 2^(l*c + nb)), nb = -(f*+1)/8), then an exact sort
 // of the last <= 64 walked in double precision, or for a larger group of
 // equal logits a cut by tie key.  above0 and limit are masses relative to the
-// row maximum; `unit` is the mass of one fixed-point unit.
+// row maximum; `unit` is the mass of one fixed-point unit.  Every
+// candidate's order key lies in [klo, khi] (the cut bin's key range).
 template <typename E>
 __device__ void resolve_candidates(ToppShared& sh, const RowSet& S, float c, float mc, int n, float nb,
-                                   double above0, double limit, double unit, uint32_t& tau, int32_t& cut,
-                                   double& K) {
+                                   double above0, double limit, double unit, uint32_t klo, uint32_t khi,
+                                   uint32_t& tau, int32_t& cut, double& K) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   unsigned long long above_f = 0;
   uint32_t kbase = 0;
   int cnt = n;
   if (n > kFinal) {
-    uint32_t kmin = 0xffffffffu, kmax = 0u;
-    for (int i = tid; i < n; i += kSThreads) {
-      const uint32_t k = order_key(sh.cand.x[i]);
-      kmin = min(kmin, k);
-      kmax = max(kmax, k);
-    }
-    kmax = static_cast<uint32_t>(block_max_u64<kSThreads>(kmax, sh.red_u));
-    kmin = 0xffffffffu - static_cast<uint32_t>(block_max_u64<kSThreads>(0xffffffffu - kmin, sh.red_u));
+    const uint32_t kmin = klo, kmax = khi;
     const double lim_rel = limit - above0;
     const unsigned long long lim_f = lim_rel > 0.0 ? static_cast<unsigned long long>(lim_rel / unit) : 0ull;
     kbase = kmin;
@@ -655,7 +657,7 @@ __device__ void resolve_candidates(ToppShared& sh, const RowSet& S, float c, flo
       __syncthreads();
       for (int i = tid; i < cnt; i += kSThreads) {
         const float x = sh.cand.x[i];
-        const uint32_t d = (order_key(x) - kbase) >> shift;
+        const uint32_t d = min((order_key(x) - kbase) >> shift, 255u);  // < 256 for keys in range
         atomicAdd(&sh.hcnt[d], 1u);
         atomicAdd(&sh.hmass[d], __float2uint_rn(ex2v(fmaf(x, c, nb)) * kFixCand));
       }
@@ -1062,12 +1064,19 @@ __global__ void __launch_bounds__(kSThreads, 5) topp_slice_kernel(StatsLaunch L)
     out[2] = Gsf;
     out[3] = 0.0f;
   }
-  __threadfence();
+  // One fence on each side, by the thread that counts the slice: the barrier
+  // orders the block's summary writes before the releasing fence, and the
+  // row's last block reads the other summaries after the acquiring fence
+  // and the barrier.
   __syncthreads();
-  if (tid == 0) sh.last = atomicAdd(L.counters + grow, 1u) == static_cast<unsigned>(ns - 1);
+  if (tid == 0) {
+    __threadfence();
+    const bool last = atomicAdd(L.counters + grow, 1u) == static_cast<unsigned>(ns - 1);
+    if (last) __threadfence();
+    sh.last = last;
+  }
   __syncthreads();
   if (!sh.last) return;
-  __threadfence();
 
   // 3. Last slice block of the row: merge the summaries.  Thread b owns the
   // row bin Gr - b; slice bins below the row's 256 go to `far`.
@@ -1254,7 +1263,8 @@ __global__ void __launch_bounds__(kSThreads, 5) topp_slice_kernel(StatsLaunch L)
         __syncthreads();
       }
       if (!generic)
-        resolve_candidates<E>(sh, S, c, mc, n, -(Bf + 1.0f) * 0.125f, above0, limit, unit, tau, cut, K);
+        resolve_candidates<E>(sh, S, c, mc, n, -(Bf + 1.0f) * 0.125f, above0, limit, unit, order_key(xlo),
+                              order_key(xhi) - 1u, tau, cut, K);
     }
     if (generic) {
       __syncthreads();
