@@ -130,6 +130,12 @@ __device__ __forceinline__ uint4 ldg_hint(const uint4* a, uint64_t pol) {
   return r;
 }
 
+// 16-byte asynchronous copy global -> shared (both 16-byte aligned).
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  const uint32_t sa = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
+}
+
 // Two bf16 logits in one 32-bit word.
 __device__ __forceinline__ __nv_bfloat162 bf2_of(uint32_t w) {
   __nv_bfloat162 r;
@@ -566,24 +572,24 @@ __device__ __forceinline__ int collect_codes(ToppShared& sh, const uint8_t* code
     }
     if (g0 + U * kSThreads < total) load(g0 + U * kSThreads);
     // Zero-byte masks of w ^ t (the top bit of each matching byte), folded
-    // into one bit per code of the batch: bit 16u + k for code k of vector u.
-    // (m >> 7) holds the four match bits at bits 0, 8, 16, 24; the product
-    // with 1 + 2^7 + 2^14 + 2^21 gathers them, without carries, at bits
-    // 21..24.
-    static_assert(U * 16 <= 32, "one bit per code of a batch");
-    uint32_t bm = 0u;
+    // into one bit per code of the batch: word i's mask shifted right by
+    // 7 - i puts the match of its byte b at bit 8b + i, so vector u's four
+    // words fill bits 32u + 8b + i (code 4i + b of the vector).  A vector of
+    // a slice without the cut bin is zero and is compared with code 1.
+    unsigned long long bm = 0ull;
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      const uint32_t t4 = t[u] >= 0 ? static_cast<uint32_t>(t[u] + 1) * 0x01010101u : 0u;  // code (t+1) mod 256
+      const uint32_t t4 = t[u] >= 0 ? static_cast<uint32_t>(t[u] + 1) * 0x01010101u : 0x01010101u;
       const uint32_t w[4] = {cv[u].x, cv[u].y, cv[u].z, cv[u].w};
+      uint32_t vm = 0u;
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const uint32_t x4 = w[i] ^ t4;
-        const uint32_t mk = t[u] >= 0 ? ~(((x4 & 0x7f7f7f7fu) + 0x7f7f7f7fu) | x4 | 0x7f7f7f7fu) : 0u;
-        bm |= ((((mk >> 7) * 0x00204081u) >> 21) & 0xfu) << (16 * u + 4 * i);
+        vm |= ~(((x4 & 0x7f7f7f7fu) + 0x7f7f7f7fu) | x4 | 0x7f7f7f7fu) >> (7 - i);
       }
+      bm |= static_cast<unsigned long long>(vm) << (32 * u);
     }
-    const int cnt = __popc(bm);
+    const int cnt = __popcll(bm);
     int incl = cnt;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -594,11 +600,12 @@ __device__ __forceinline__ int collect_codes(ToppShared& sh, const uint8_t* code
     // One loop over the set bits (its trip count is the lane's count, not
     // one loop per word).
     while (bm) {
-      const int k = __ffs(bm) - 1;
+      const int k = __ffsll(static_cast<long long>(bm)) - 1;
       bm &= bm - 1;
-      const int g = g0 + (k >> 4) * kSThreads + tid;
+      const int g = g0 + (k >> 5) * kSThreads + tid;
       const int q = g >> kQShift;
-      if (slot < kRegion) region[slot] = rs.head + q * SL + (g & (Q16 - 1)) * 16 + (k & 15);
+      const int e = 4 * (k & 7) + ((k >> 3) & 3);  // code of the vector
+      if (slot < kRegion) region[slot] = rs.head + q * SL + (g & (Q16 - 1)) * 16 + e;
       ++slot;
     }
     wn += __shfl_sync(0xffffffffu, incl, 31);
@@ -1081,18 +1088,29 @@ __global__ void __launch_bounds__(kSThreads, 5) topp_slice_kernel(StatsLaunch L)
   // 3. Last slice block of the row: merge the summaries.  Thread b owns the
   // row bin Gr - b; slice bins below the row's 256 go to `far`.
   const float* sum0 = L.summ + static_cast<int64_t>(sbase) * kSummary;
-  // Slice maxima and top bins, staged in shared memory when they fit.
-  const bool staged = ns <= kMaxStaged;
+  // The row's slice summaries land in shared memory (one round of
+  // asynchronous copies; they span the candidate arrays, free until the
+  // candidates are collected) when they fit; else they are read through L2,
+  // the slice maxima and top bins staged in shared memory.
+  float* ss = reinterpret_cast<float*>(&sh.cand);
+  const bool in_smem = ns * kSummary <= 2 * kCandCap;
+  if (in_smem) {
+    const int n16 = ns * (kSummary / 4);
+    for (int i = tid; i < n16; i += kSThreads) cp_async16(ss + 4 * i, sum0 + 4 * i);
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    __syncthreads();
+  }
+  auto ldsum = [&](int64_t i) -> float { return in_smem ? ss[i] : __ldcg(sum0 + i); };
+  const bool staged = !in_smem && ns <= kMaxStaged;
   float* hm = sh.cand.x;               // slice maximum
   float* hg = sh.cand.x + kMaxStaged;  // slice top bin
   float m = -CUDART_INF_F;
   for (int q = tid; q < ns; q += kSThreads) {
-    const float* sq = sum0 + static_cast<int64_t>(q) * kSummary;
-    const float mq = __ldcg(sq);
+    const float mq = ldsum(static_cast<int64_t>(q) * kSummary);
     m = fmaxf(m, mq);
     if (staged) {
       hm[q] = mq;
-      hg[q] = __ldcg(sq + 2);
+      hg[q] = __ldcg(sum0 + static_cast<int64_t>(q) * kSummary + 2);
     }
   }
   m = block_max<kSThreads>(m, sh.red_f);  // its barriers also publish the staging
@@ -1131,14 +1149,14 @@ __global__ void __launch_bounds__(kSThreads, 5) topp_slice_kernel(StatsLaunch L)
     } else {
 #pragma unroll 1
       for (int q = 0; q < ns; ++q) {
-        const float* sq = sum0 + static_cast<int64_t>(q) * kSummary;
-        const float mq = __ldcg(sq);
+        const int64_t sq = static_cast<int64_t>(q) * kSummary;
+        const float mq = ldsum(sq);
         if (!(mq > -CUDART_INF_F)) continue;
-        const float Gq = __ldcg(sq + 2);
+        const float Gq = ldsum(sq + 2);
         const int D = static_cast<int>(Grf - Gq);
-        if (tid >= D && tid < kNB) acc += static_cast<unsigned long long>(__ldcg(sq + 4 + (tid - D)));
+        if (tid >= D && tid < kNB) acc += static_cast<unsigned long long>(ldsum(sq + 4 + (tid - D)));
         if (tid >= kNB - D && tid < kNB)
-          farp += __ldcg(sq + 4 + tid) * ex2v((Gq - static_cast<float>(tid) + 1.0f) * 0.125f - mc - kFixL2);
+          farp += ldsum(sq + 4 + tid) * ex2v((Gq - static_cast<float>(tid) + 1.0f) * 0.125f - mc - kFixL2);
       }
     }
     // Mass of one unit of bin Gr - b: 2^((Gr - b + 1)/8 - kFixLog2 - mc), with the
@@ -1191,9 +1209,9 @@ __global__ void __launch_bounds__(kSThreads, 5) topp_slice_kernel(StatsLaunch L)
       __syncthreads();
       for (int q = tid; q < ns && q < kNB; q += kSThreads) {
         int t = -1;
-        const float mq = staged ? hm[q] : __ldcg(sum0 + static_cast<int64_t>(q) * kSummary);
+        const float mq = staged ? hm[q] : ldsum(static_cast<int64_t>(q) * kSummary);
         if (mq > -CUDART_INF_F) {
-          const float Gq = staged ? hg[q] : __ldcg(sum0 + static_cast<int64_t>(q) * kSummary + 2);
+          const float Gq = staged ? hg[q] : ldsum(static_cast<int64_t>(q) * kSummary + 2);
           t = gstar - static_cast<int>(Grf - Gq);
           if (t >= kNB - 1) sh.ncand = 1;
         }
