@@ -11,6 +11,8 @@
 // §七 (--temp 0 benchmarking); "A 2.16x speculative-decoding speedup from a
 // 1-layer Llama draft", headline table ("Match = True": greedy speculative
 // output equals greedy decoding) and §5 (draft token tree).
+#include <cuda_bf16.h>
+
 #include "sv_internal.h"
 
 namespace sv {
@@ -44,6 +46,27 @@ struct GreedyParams {
   // sample
   float* out_prob;
 };
+
+// The largest logit of one 16-byte vector (bf16: packed maxima, two logits
+// per instruction; fp32: three-input maxima).  A NaN never hides a number,
+// as with fmaxf.
+template <typename E>
+__device__ __forceinline__ float vec_max(const uint4& w) {
+  if constexpr (sizeof(E) == 2) {
+    auto h = [](uint32_t x) {
+      __nv_bfloat162 r;
+      memcpy(&r, &x, sizeof(r));
+      return r;
+    };
+    const __nv_bfloat162 m = __hmax2(__hmax2(h(w.x), h(w.y)), __hmax2(h(w.z), h(w.w)));
+    return fmaxf(__low2float(m), __high2float(m));
+  } else {
+    float m;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(m) : "f"(__uint_as_float(w.x)), "f"(__uint_as_float(w.y)),
+        "f"(__uint_as_float(w.z)));
+    return fmaxf(m, __uint_as_float(w.w));
+  }
+}
 
 // Largest value with the lowest index over one row, packed (see argmax_pack);
 // the result is valid in every thread.
@@ -80,12 +103,12 @@ __device__ __forceinline__ unsigned long long row_argmax(const E* row, int V, in
     }
 #pragma unroll
     for (int u = 0; u < UNROLL; ++u) {
-      float x[EPV];
-      unpack<E>(buf[u], x);
-      float vm = x[0];
-#pragma unroll
-      for (int i = 1; i < EPV; ++i) vm = fmaxf(vm, x[i]);
+      // The vector's maximum by packed maxima (bf16: two logits per
+      // instruction); its lowest index only when it beats the running one.
+      const float vm = vec_max<E>(buf[u]);
       if (vm > bv) {
+        float x[EPV];
+        unpack<E>(buf[u], x);
         int first = EPV - 1;
 #pragma unroll
         for (int i = EPV - 1; i >= 0; --i)
