@@ -17,19 +17,22 @@
 //    upper edge, v = round(2^F * 2^(l*c - (f+1)/8)) (F = 21 for fp32, 20 for
 //    bf16 rows), summed exactly in
 //    per-warp u32 histograms (shared-memory integer reductions, no read-
-//    modify-write chains); lower logits count in the lowest bin.  The block
-//    publishes (m_s, top bin, 256 bin sums) and bumps the row's counter;
+//    modify-write chains); lower logits count in the lowest bin.  Two logits
+//    are binned per packed FP32 instruction.  Every logit's bin slot is also
+//    stored as one code byte, in logit order.  The block publishes (m_s, top
+//    bin, 256 bin sums) and bumps the row's counter;
 //  * the row's last slice block merges the summaries (a bin's mass is its
 //    summed v times 2^((f+1)/8 - F - m*c) whichever slice it came from),
 //    finds the bin f* where the mass from the top first exceeds top_p * S,
-//    rescans the row (just read by its sibling blocks, so served by L2) to
-//    collect the logits of f* with their ids in shared memory, and resolves
-//    the cut among them by radix levels over their order keys, ending with
-//    an exact sort of the last <= 64 by (logit descending, tie key ascending)
-//    walked in double precision.
+//    finds the logits of f* from the code bytes (a quarter of an fp32 row's
+//    bytes) and gathers their values, and resolves the cut among them by
+//    radix levels over their order keys, ending with an exact sort of the
+//    last <= 64 by (logit descending, tie key ascending) walked in double
+//    precision.
 // Rare rows (the cut in the lowest of the 256 bins under the maximum or
-// below, more than 4096 logits in f*) take an exact radix select over the
-// order keys of the row.
+// below, a slice whose lowest bin holds f*, more than 4096 logits in f*)
+// rescan the row's values or take an exact radix select over the order keys
+// of the row.
 #include "sv_rows.cuh"
 
 #include <cuda_bf16.h>
