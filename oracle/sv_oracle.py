@@ -269,7 +269,8 @@ def verify_chain_row(target_logits: np.ndarray, draft_logits: np.ndarray | None,
     computed; inf otherwise), p_alts / q_alts [γ, ALTS] (p_i(d_i) and
     q_i(d_i) under every admissible cut, the oracle's own first; NaN padded),
     final_alts [ALTS^2] (every token the draw at k gives under the admissible
-    cuts of rows k, the oracle's own first; -1 padded), status,
+    cuts of rows k, the oracle's own first; at T == 0 the argmax g_k alone;
+    -1 padded), status,
     resample_fallback (bool: residual mass was 0)).
 
     Margins and alternatives (reporting only; no result depends on them).  A
@@ -307,6 +308,7 @@ def verify_chain_row(target_logits: np.ndarray, draft_logits: np.ndarray | None,
                 break
         tokens[:k] = ids[:k]
         tokens[k] = g[k]
+        res["final_alts"][0] = g[k]
         res["k"] = k
         return res
 

@@ -88,8 +88,9 @@ def compare_chain(got: dict, want: dict, ids: np.ndarray, dtype: str, rows=None,
     for b in rows:
         k = int(want["num_accepted"][b])
         alts = want["final_alts"][b] if "final_alts" in want else want["tokens"][b, k:k + 1]
+        alts = alts[alts >= 0] if np.any(alts >= 0) else want["tokens"][b, k:k + 1]  # greedy and status rows
         same = (got["num_accepted"][b] == k and np.array_equal(got["tokens"][b, :k], want["tokens"][b, :k])
-                and int(got["tokens"][b, k]) in alts[alts >= 0].tolist()
+                and int(got["tokens"][b, k]) in alts.tolist()
                 and np.array_equal(got["tokens"][b, k + 1:], want["tokens"][b, k + 1:]))
         st_got = int(got["row_status"][b]) & ~32
         st_want = int(want["status"][b])
@@ -103,7 +104,7 @@ def compare_chain(got: dict, want: dict, ids: np.ndarray, dtype: str, rows=None,
             assert min(int(got["num_accepted"][b]), nf) == min(k, nf), (b, nf)
         else:
             assert same, (f"row {b}: tokens {got['tokens'][b]} k={got['num_accepted'][b]} vs oracle "
-                          f"{want['tokens'][b]} k={k} (or {alts[alts >= 0]}) margin={want['margin'][b]:.3g}")
+                          f"{want['tokens'][b]} k={k} (or {alts}) margin={want['margin'][b]:.3g}")
         if check_probs and "p_draft" in got and st_want == 0:
             G = got["p_draft"].shape[1]
             for key in ("p", "q"):

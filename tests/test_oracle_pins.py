@@ -408,3 +408,10 @@ def test_chain_residual_draw_under_admissible_cuts():
     assert r["final_alts"].tolist() == [2, 1] + [-1] * 7
     assert r["margin"] == pytest.approx(min(0.9 - 0.625, 0.7 - 2 / 3), rel=1e-12)
     assert not r["resample_fallback"]
+
+
+def test_greedy_row_lists_its_one_final_token():
+    t = np.stack([_row_of(PROBS)] * 3)
+    r = O.verify_chain_row(t, None, np.array([0, 1]), None, None, 0.0, 1.0)
+    assert r["k"] == 1 and r["tokens"].tolist() == [0, 0, -1]
+    assert r["final_alts"].tolist() == [0] + [-1] * 8
