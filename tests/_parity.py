@@ -114,9 +114,11 @@ def compare_chain(got: dict, want: dict, ids: np.ndarray, dtype: str, rows=None,
                 err = np.abs(g[:, None] - w) / np.maximum(np.abs(w), 1e-300)
                 hit = (np.abs(g[:, None] - w) <= ATOL) | (err <= TOL[dtype])   # NaN pads never hit
                 assert hit.any(axis=1).all(), (b, key, g, w)
-                # error against the closest admissible value, where it is not tiny
-                e = np.where(np.isnan(err) | (np.abs(w) <= 1e-9), np.inf, err).min(axis=1)
-                e = e[np.isfinite(e)]
+                # relative error against the closest admissible value (0 where an
+                # absolute match within ATOL), over positions with a non-tiny value
+                ea = np.where(np.abs(g[:, None] - w) <= ATOL, 0.0, err)
+                e = np.where(np.isnan(ea), np.inf, ea).min(axis=1)
+                e = e[np.isfinite(e) & (np.nanmax(np.abs(w), axis=1) > 1e-9)]
                 if e.size:
                     max_rel = max(max_rel, float(e.max()))
     return len(rows), n_near, n_near_mis, max_rel

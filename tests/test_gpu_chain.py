@@ -124,6 +124,39 @@ def test_qwen3_d2t_every_batch_row(sv, qwen3):
     assert near_mis <= len(done) // 50, near_mis
 
 
+def test_top_p_cut_at_the_threshold(sv):
+    """Rows whose top-p cut lies within 1e-8 of top_p: three ids with masses
+    0.5, 0.3, 0.2 in some order (the same ids in target and draft row i; the
+    other 4093 logits e^-30 below) at top_p = 0.8, so whether the third id
+    is kept is decided by rounding.  The oracle takes
+    every accept test and the draw under both cuts; the library's tokens must
+    be among those it admits, its p/q within tolerance of one cut's value."""
+    V, G, B = 4096, 3, 64
+    x = _case(V, G, "f32", 1.0, 0.8, ties=False, B=B, seed=77)
+    rng = np.random.default_rng(77)
+    tgt = np.full((B, G + 1, V), -30.0, np.float32)
+    dft = np.full((B, G, V), -30.0, np.float32)
+    for b in range(B):
+        for i in range(G + 1):
+            three = rng.choice(V, 3, replace=False)
+            # the same three ids in target and draft row i, masses in another order
+            tgt[b, i, three] = np.log(rng.permutation([0.5, 0.3, 0.2])).astype(np.float32)
+            if i < G:
+                dft[b, i, three] = np.log(rng.permutation([0.5, 0.3, 0.2])).astype(np.float32)
+    for key, a in (("target", tgt), ("draft", dft)):
+        x[key] = a
+        x[key + "_store"] = a
+    ids = oracle_draft_ids(x)
+    got = run_chain(sv, x, ids)
+    want = oracle_chain(x, ids)
+    # every row has the shorter cut as an alternative
+    assert np.isfinite(want["p_alts"][:, :, 1]).all() and np.isfinite(want["q_alts"][:, :, 1]).all()
+    multi = int(((want["final_alts"] >= 0).sum(axis=1) > 1).sum())
+    res = compare_chain(got, want, ids, "f32")
+    _report(f"top-p cut at the threshold, {multi} rows with two admissible draws", res)
+    assert multi > 0
+
+
 def test_qwen3_d2t_repeat_is_identical(sv, qwen3):
     """Two calls in a row give the same bits (deterministic, workspace reset)."""
     x, ids = qwen3
