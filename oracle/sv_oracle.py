@@ -444,19 +444,36 @@ def verify_chain(target_logits, draft_logits, draft_ids, u_accept, u_resample,
 # ---------------------------------------------------------------------------
 
 def sample_row(logits: np.ndarray, temperature: float, top_p: float, u: float,
-               tie_index: np.ndarray | None = None):
+               tie_index: np.ndarray | None = None, alts: list | None = None):
     """One token from dist(logits, T, top_p) with the uniform u.
 
     [P3] §4.2 draft loop: ``/ temperature`` -> ``_apply_top_p`` -> softmax ->
     ``multinomial``; T == 0 is the argmax (lowest index on ties).
-    Returns (token, margin).
+    Returns (token, margin); the margin includes the top-p cut's own.
+
+    When ``alts`` is a list (reporting only, as for the chain verify's
+    final_alts) it receives (token, its probability) for the oracle's own cut
+    and for every other cut within NEAR of top_p (top_p_filter's "alts"), and
+    the margin returned is the draw's smallest margin over those cuts, without
+    the cut's own.
     """
     logits = np.asarray(logits, dtype=np.float64)
     if temperature == 0.0:
-        return int(np.argmax(logits)), np.inf
-    p, mg_top = dist(logits, temperature, top_p, tie_index)
+        tok = int(np.argmax(logits))
+        if alts is not None:
+            alts.append((tok, 1.0))
+        return tok, np.inf
+    cut = {} if alts is not None else None
+    p, mg_top = dist(logits, temperature, top_p, tie_index, cut=cut)
     tok, mg = inverse_cdf(p, u)
-    return tok, min(mg, mg_top)
+    if alts is None:
+        return tok, min(mg, mg_top)
+    alts.append((tok, float(p[tok])))
+    for q in cut["alts"]:
+        t2, m2 = inverse_cdf(q, u)
+        alts.append((t2, float(q[t2])))
+        mg = min(mg, m2)
+    return tok, mg
 
 
 # ---------------------------------------------------------------------------

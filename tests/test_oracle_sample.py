@@ -159,3 +159,23 @@ def test_compact_row_ties_follow_the_target_ids():
     for u in (0.0, 0.3, 0.7, 0.999):
         assert O.sample_row(logits, 1.0, 0.3, u, tie_index=tie_index)[0] == 1
     assert O.sample_row(logits, 1.0, 0.3, 0.5)[0] == 0
+
+
+def test_sample_row_lists_the_draws_of_admissible_cuts():
+    """Masses 0.5, 0.3, 0.15, 0.05 (cum 0.5, 0.8, 0.95, 1.0) and top_p 1e-9
+    above 0.8: the cut keeps three ids, or two.  u = 0.55 draws id 1 under
+    the own cut (its interval [0.5/0.95, 0.8/0.95]) and id 0 under the
+    shorter one ([0, 0.625]); the margin is the smaller distance to an edge."""
+    row = np.log(np.array([0.5, 0.3, 0.15, 0.05]))
+    alts = []
+    tok, mg = O.sample_row(row, 1.0, 0.8 + 1e-9, 0.55, alts=alts)
+    assert tok == 1
+    assert [a[0] for a in alts] == [1, 0]
+    assert alts[0][1] == pytest.approx(0.3 / 0.95, rel=1e-12) and alts[1][1] == pytest.approx(0.625, rel=1e-12)
+    assert mg == pytest.approx(0.55 - 0.5 / 0.95, rel=1e-12)
+    # without the list, the cut's own margin (1e-9) decides
+    assert O.sample_row(row, 1.0, 0.8 + 1e-9, 0.55)[1] < 1e-8
+    # far from any cut: one admissible draw
+    alts = []
+    O.sample_row(row, 1.0, 0.9, 0.55, alts=alts)
+    assert len(alts) == 1
