@@ -11,9 +11,11 @@
 namespace sv {
 
 // Gather form: every output element is written exactly once,
-// out[r, t] = t2d[t] >= 0 ? in[r, t2d[t]] : fill.  One thread per 16-byte
-// output vector; t2d is read as int4.
-template <typename E, int THREADS>
+// out[r, t] = t2d[t] >= 0 ? in[r, t2d[t]] : fill.  Each thread owns U
+// 16-byte output vectors of its row (strided by the block, so every load and
+// store is coalesced); all their t2d entries are loaded before any value is
+// gathered, and every gather before any store.
+template <typename E, int THREADS, int U>
 __global__ void __launch_bounds__(THREADS)
 scatter_gather_kernel(const E* __restrict__ in, int64_t in_stride, const int32_t* __restrict__ t2d,
                       int vd, int V, E fill, E* __restrict__ out, int64_t out_stride, int tiles) {
@@ -22,30 +24,49 @@ scatter_gather_kernel(const E* __restrict__ in, int64_t in_stride, const int32_t
   const int tile = blockIdx.x - row * tiles;
   const E* src = in + static_cast<int64_t>(row) * in_stride;
   E* dst = out + static_cast<int64_t>(row) * out_stride;
-  const int v = tile * THREADS + threadIdx.x;
-  const int t0 = v * EPV;
   const bool vec_ok = ((reinterpret_cast<uintptr_t>(dst) | reinterpret_cast<uintptr_t>(t2d)) & 15u) == 0;
-  if (vec_ok && t0 + EPV <= V) {
-    int32_t ids[EPV];
+  const int v0 = tile * THREADS * U + static_cast<int>(threadIdx.x);
+  if (vec_ok) {
+    int32_t ids[U][EPV];
 #pragma unroll
-    for (int q = 0; q < EPV / 4; ++q) {
-      const int4 w = __ldg(reinterpret_cast<const int4*>(t2d + t0) + q);
-      ids[4 * q + 0] = w.x;
-      ids[4 * q + 1] = w.y;
-      ids[4 * q + 2] = w.z;
-      ids[4 * q + 3] = w.w;
-    }
-    E vals[EPV];
+    for (int u = 0; u < U; ++u) {
+      const int t0 = (v0 + u * THREADS) * EPV;
 #pragma unroll
-    for (int e = 0; e < EPV; ++e) {
-      const int j = ids[e];
-      vals[e] = (j >= 0 && j < vd) ? src[j] : fill;
+      for (int q = 0; q < EPV / 4; ++q) {
+        const int4 w = t0 + EPV <= V ? __ldg(reinterpret_cast<const int4*>(t2d + t0) + q) : make_int4(-1, -1, -1, -1);
+        ids[u][4 * q + 0] = w.x;
+        ids[u][4 * q + 1] = w.y;
+        ids[u][4 * q + 2] = w.z;
+        ids[u][4 * q + 3] = w.w;
+      }
     }
-    *reinterpret_cast<uint4*>(dst + t0) = *reinterpret_cast<const uint4*>(vals);
-  } else if (t0 < V) {
-    for (int t = t0; t < min(V, t0 + EPV); ++t) {
-      const int j = t2d[t];
-      dst[t] = (j >= 0 && j < vd) ? src[j] : fill;
+    E vals[U][EPV];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) {
+        const int j = ids[u][e];
+        vals[u][e] = (j >= 0 && j < vd) ? src[j] : fill;
+      }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int t0 = (v0 + u * THREADS) * EPV;
+      if (t0 + EPV <= V) {
+        *reinterpret_cast<uint4*>(dst + t0) = *reinterpret_cast<const uint4*>(vals[u]);
+      } else {
+        for (int t = t0; t < V; ++t) {
+          const int j = t2d[t];
+          dst[t] = (j >= 0 && j < vd) ? src[j] : fill;
+        }
+      }
+    }
+  } else {
+    for (int u = 0; u < U; ++u) {
+      const int t0 = (v0 + u * THREADS) * EPV;
+      for (int t = t0; t < min(V, t0 + EPV); ++t) {
+        const int j = t2d[t];
+        dst[t] = (j >= 0 && j < vd) ? src[j] : fill;
+      }
     }
   }
 }
@@ -118,9 +139,11 @@ static sv_status scatter_impl(const void* in, int64_t in_stride, const int32_t* 
   if (rows == 0) return SV_OK;
   const E f = to_elem<E>(fill);
   if (t2d) {
+    constexpr int kU = 8;
     const int nv = (V + Elem<E>::kPerVec - 1) / Elem<E>::kPerVec;
-    const int tiles = (nv + kThreads - 1) / kThreads;
-    scatter_gather_kernel<E, kThreads><<<static_cast<unsigned>(rows) * tiles, kThreads, 0, stream>>>(
+    const int tiles = (nv + kThreads * kU - 1) / (kThreads * kU);
+    if (static_cast<long long>(rows) * tiles > INT32_MAX) return SV_ERR_UNSUPPORTED;
+    scatter_gather_kernel<E, kThreads, kU><<<static_cast<unsigned>(rows) * tiles, kThreads, 0, stream>>>(
         static_cast<const E*>(in), in_stride, t2d, vd, V, f, static_cast<E*>(out), out_stride, tiles);
   } else {
     scatter_fill_kernel<E, 1024><<<rows, 1024, 0, stream>>>(static_cast<const E*>(in), in_stride, d2t,

@@ -116,6 +116,38 @@ def test_d2t_scatter_matches_oracle(sv, dtype, shuffled, with_t2d):
     np.testing.assert_array_equal(out.float().cpu().numpy(), want.astype(np.float32))
 
 
+@pytest.mark.parametrize("with_t2d", [True, False])
+def test_d2t_scatter_full_draft_set(sv, with_t2d):
+    """Every draft row of the Qwen3/EAGLE3 workload (256 x 7 rows of 32000
+    fp32 logits into 151936 ids) in one call: sampled rows equal the oracle's
+    scatter, and every other row is its draft row at the mapped ids and the
+    fill elsewhere (checked on the device)."""
+    import torch
+    V, Vd, R = 151936, 32000, 256 * 7
+    d2t = synth.make_d2t(7, V, Vd, shuffled=True)
+    g = torch.Generator(device="cuda").manual_seed(7)
+    x = torch.randn((R, Vd), generator=g, device="cuda") * 2.0
+    d2t_t = t(d2t)
+    t2d = sv.build_t2d(d2t_t, V)[0] if with_t2d else None
+    out = sv.d2t_scatter(x, d2t_t, V, fill=-math.inf, t2d=t2d)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    sv.d2t_scatter(x, d2t_t, V, fill=-math.inf, t2d=t2d, out=out)
+    end.record()
+    torch.cuda.synchronize()
+    ms = start.elapsed_time(end)
+    print(f"[d2t scatter {'gather form' if with_t2d else 'fill form'}] {R} rows: {ms * 1e3:.1f} us, "
+          f"{R * (V + Vd) * 4 / (ms * 1e-3) / 1e12:.2f} TB/s (rows read once, written once)")
+    rows = np.random.default_rng(3).choice(R, 8, replace=False)
+    xs = x[torch.from_numpy(rows).cuda()].cpu().numpy()
+    np.testing.assert_array_equal(out[torch.from_numpy(rows).cuda()].cpu().numpy(), O.d2t_scatter(xs, d2t, V))
+    idx = d2t_t.long()
+    assert torch.equal(out[:, idx], x)
+    mask = torch.ones(V, dtype=torch.bool, device="cuda")
+    mask[idx] = False
+    assert bool(torch.isneginf(out[:, mask]).all())
+
+
 def test_d2t_scatter_odd_sizes_and_fill(sv):
     import torch
     V, Vd, R = 1001, 37, 3
