@@ -71,29 +71,87 @@ scatter_gather_kernel(const E* __restrict__ in, int64_t in_stride, const int32_t
   }
 }
 
-// Scatter form (no t2d): one block per row fills the row, then writes the
-// draft values at their target ids.  The barrier orders the two phases.
+// Sum of one int per thread, valid in every thread (shared counter: zeroed,
+// added to, read; three barriers).
+template <int THREADS>
+__device__ __forceinline__ int block_sum_i(int v, int* counter) {
+  if (threadIdx.x == 0) *counter = 0;
+  __syncthreads();
+  if (v) atomicAdd(counter, v);
+  __syncthreads();
+  const int r = *counter;
+  __syncthreads();
+  return r;
+}
+
+// Scatter form (no t2d): one block per row.  When d2t is strictly
+// increasing within [0, V) (checked by the block over the whole map, which
+// stays in L2), the row is built in shared-memory tiles of kTile ids: a
+// tile is set to `fill`, the draft values whose ids fall in it (a contiguous
+// run of draft ids, the run advancing tile by tile) are placed, and the tile
+// is written out once with 16-byte stores.  Otherwise the block fills the
+// row, then writes the draft values at their target ids (the barrier orders
+// the two phases; every row is written twice).
 template <typename E, int THREADS>
 __global__ void __launch_bounds__(THREADS)
 scatter_fill_kernel(const E* __restrict__ in, int64_t in_stride, const int32_t* __restrict__ d2t,
                     int vd, int V, E fill, E* __restrict__ out, int64_t out_stride) {
   constexpr int EPV = Elem<E>::kPerVec;
+  constexpr int kTile = 8192;
+  __shared__ __align__(16) E tile[kTile];
+  __shared__ int s_a;
   const int row = blockIdx.x;
   const E* src = in + static_cast<int64_t>(row) * in_stride;
   E* dst = out + static_cast<int64_t>(row) * out_stride;
-  E fv[EPV];
-#pragma unroll
-  for (int e = 0; e < EPV; ++e) fv[e] = fill;
-  const uint4 fvec = *reinterpret_cast<const uint4*>(fv);
-  const RowSplit rs = split_row(dst, V);
-  uint4* dv = reinterpret_cast<uint4*>(dst + rs.head);
-  for (int v = threadIdx.x; v < rs.nvec; v += THREADS) dv[v] = fvec;
-  for (int t = threadIdx.x; t < rs.head; t += THREADS) dst[t] = fill;
-  for (int t = rs.tail0 + threadIdx.x; t < V; t += THREADS) dst[t] = fill;
-  __syncthreads();
+  int bad = 0;
   for (int j = threadIdx.x; j < vd; j += THREADS) {
     const int x = __ldg(d2t + j);
-    if (x >= 0 && sv_in(x, V)) dst[x] = src[j];
+    if (x < 0 || x >= V || (j + 1 < vd && __ldg(d2t + j + 1) <= x)) bad = 1;
+  }
+  if (__syncthreads_or(bad)) {
+    E fv[EPV];
+#pragma unroll
+    for (int e = 0; e < EPV; ++e) fv[e] = fill;
+    const uint4 fvec = *reinterpret_cast<const uint4*>(fv);
+    const RowSplit rs = split_row(dst, V);
+    uint4* dv = reinterpret_cast<uint4*>(dst + rs.head);
+    for (int v = threadIdx.x; v < rs.nvec; v += THREADS) dv[v] = fvec;
+    for (int t = threadIdx.x; t < rs.head; t += THREADS) dst[t] = fill;
+    for (int t = rs.tail0 + threadIdx.x; t < V; t += THREADS) dst[t] = fill;
+    __syncthreads();
+    for (int j = threadIdx.x; j < vd; j += THREADS) {
+      const int x = __ldg(d2t + j);
+      if (x >= 0 && sv_in(x, V)) dst[x] = src[j];
+    }
+    return;
+  }
+  const bool vec_ok = (reinterpret_cast<uintptr_t>(dst) & 15u) == 0;
+  int a = 0;  // the first draft id whose target id is at or past this tile
+  for (int t0 = 0; t0 < V; t0 += kTile) {
+    const int n = min(kTile, V - t0);
+    for (int i = threadIdx.x; i < n; i += THREADS) tile[i] = fill;
+    __syncthreads();
+    // The draft ids of this tile are a contiguous run from a (d2t is
+    // increasing), at most n of them: place them and count them.
+    const int m = min(n, vd - a);
+    int cnt = 0;
+    for (int i = threadIdx.x; i < m; i += THREADS) {
+      const int x = __ldg(d2t + a + i) - t0;
+      if (x < n) {
+        if (sv_in(x, n)) tile[x] = src[a + i];
+        ++cnt;
+      }
+    }
+    const int run = block_sum_i<THREADS>(cnt, &s_a);  // its barriers also publish the tile
+    if (vec_ok && (n % EPV) == 0 && (t0 % EPV) == 0) {
+      const uint4* tv = reinterpret_cast<const uint4*>(tile);
+      uint4* dv = reinterpret_cast<uint4*>(dst + t0);
+      for (int v = threadIdx.x; v < n / EPV; v += THREADS) dv[v] = tv[v];
+    } else {
+      for (int i = threadIdx.x; i < n; i += THREADS) dst[t0 + i] = tile[i];
+    }
+    __syncthreads();
+    a += run;
   }
 }
 

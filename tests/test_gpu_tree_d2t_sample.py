@@ -116,15 +116,16 @@ def test_d2t_scatter_matches_oracle(sv, dtype, shuffled, with_t2d):
     np.testing.assert_array_equal(out.float().cpu().numpy(), want.astype(np.float32))
 
 
-@pytest.mark.parametrize("with_t2d", [True, False])
-def test_d2t_scatter_full_draft_set(sv, with_t2d):
+@pytest.mark.parametrize("with_t2d,shuffled", [(True, False), (False, False), (False, True)])
+def test_d2t_scatter_full_draft_set(sv, with_t2d, shuffled):
     """Every draft row of the Qwen3/EAGLE3 workload (256 x 7 rows of 32000
     fp32 logits into 151936 ids) in one call: sampled rows equal the oracle's
-    scatter, and every other row is its draft row at the mapped ids and the
-    fill elsewhere (checked on the device)."""
+    scatter, and every row is its draft row at the mapped ids and the fill
+    elsewhere (checked on the device).  An increasing d2t (EAGLE3's) takes
+    the tiled fill form without t2d; a shuffled one the two-phase form."""
     import torch
     V, Vd, R = 151936, 32000, 256 * 7
-    d2t = synth.make_d2t(7, V, Vd, shuffled=True)
+    d2t = synth.make_d2t(7, V, Vd, shuffled=shuffled)
     g = torch.Generator(device="cuda").manual_seed(7)
     x = torch.randn((R, Vd), generator=g, device="cuda") * 2.0
     d2t_t = t(d2t)
@@ -136,7 +137,8 @@ def test_d2t_scatter_full_draft_set(sv, with_t2d):
     end.record()
     torch.cuda.synchronize()
     ms = start.elapsed_time(end)
-    print(f"[d2t scatter {'gather form' if with_t2d else 'fill form'}] {R} rows: {ms * 1e3:.1f} us, "
+    form = "gather form" if with_t2d else ("fill form, shuffled d2t" if shuffled else "fill form, increasing d2t")
+    print(f"[d2t scatter {form}] {R} rows: {ms * 1e3:.1f} us, "
           f"{R * (V + Vd) * 4 / (ms * 1e-3) / 1e12:.2f} TB/s (rows read once, written once)")
     rows = np.random.default_rng(3).choice(R, 8, replace=False)
     xs = x[torch.from_numpy(rows).cuda()].cpu().numpy()
