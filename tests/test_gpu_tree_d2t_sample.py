@@ -177,6 +177,42 @@ def test_build_t2d(sv):
     assert st.item() & 1
 
 
+@pytest.mark.parametrize("dtype,V,top_p", [("f32", 32000, 0.95), ("bf16", 49152, 0.9), ("bf16", 128256, 1.0)])
+def test_sample_rows_full_size(sv, dtype, V, top_p):
+    """Draft-side sampling of 1792 rows at once (the qwen3 draft rows'
+    count: 32000 fp32 at top_p 0.95; 49152 bf16 at 0.9; 128256 bf16 without
+    top-p), timed; sampled rows against the oracle's admissible draws."""
+    import torch
+    R, T = 1792, 1.0
+    g = torch.Generator(device="cuda").manual_seed(V)
+    x = torch.randn((R, V), generator=g, device="cuda") * 2.5
+    if dtype == "bf16":
+        x = x.to(torch.bfloat16)
+    u = torch.rand(R, generator=g, device="cuda")
+    tok, prob = sv.sample(x, T, top_p, u)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    tok, prob = sv.sample(x, T, top_p, u)
+    end.record()
+    torch.cuda.synchronize()
+    ms = start.elapsed_time(end)
+    es = 2 if dtype == "bf16" else 4
+    print(f"[sample {R} x {V} {dtype} top_p={top_p}] {ms * 1e3:.1f} us, {R * V * es / (ms * 1e-3) / 1e12:.2f} TB/s "
+          "(rows read once; the draw re-reads one chunk per row)")
+    rows = np.random.default_rng(V).choice(R, 8, replace=False)
+    xs = x[torch.from_numpy(rows).cuda()].float().cpu().numpy()
+    us = u[torch.from_numpy(rows).cuda()].cpu().numpy()
+    checked = 0
+    for i, r in enumerate(rows):
+        alts = []
+        want, margin = O.sample_row(xs[i], T, top_p, float(us[i]), alts=alts)
+        if margin < O.NEAR:
+            continue
+        assert int(tok[r]) in [a for a, _ in alts], (r, int(tok[r]), alts)
+        checked += 1
+    assert checked >= 4, checked
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("V,T,top_p", [(1, 1.0, 0.9), (3, 0.5, 1.0), (1000, 0.8, 0.9), (49152, 0.8, 0.9),
                                        (32000, 1.0, 0.95), (4097, 0.0, 1.0), (128256, 1.0, 1.0)])
