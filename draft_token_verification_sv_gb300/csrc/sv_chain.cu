@@ -246,9 +246,234 @@ sv_status sampling_chain(const ChainArgs& a, cudaStream_t stream) {
   return launch_decide(P, d.target_dtype, d.draft_dtype, static_cast<char*>(a.workspace) + WL.decide, stream);
 }
 
+// Sampling without top-p in one pass over each row (one block per row):
+// every warp reduces whole chunks of 2048 ids to (chunk maximum m_c, sum of
+// exp2((l - m_c) c)); the block combines the
+// chunks into the row's maximum M and total S (double), takes the chunk
+// holding u * S by a prefix over the chunks' masses in ascending id order,
+// and rescans that chunk alone (just read: L2) with a block prefix scan in
+// double.  Draw as the inverse CDF ("LLM inference acceleration in practice
+// ..." §4.2 `multinomial`): the first id whose inclusive prefix exceeds u * S;
+// zero-mass ids are never drawn; if rounding leaves u * S at or above the
+// total, the last finite id.  Rows aligned to 16 bytes, V a multiple of the
+// vector width and at most kSampleMaxChunks chunks.
+constexpr int kSampleThreads = 512;
+constexpr int kSampleChunk = 2048;
+constexpr int kSampleMaxChunks = 512;
+
+template <typename E>
+__global__ void __launch_bounds__(kSampleThreads, 2) sample_stream_kernel(const E* __restrict__ logits, int64_t stride,
+                                                                     int V, float c, const float* __restrict__ u,
+                                                                     int32_t* out_tokens, float* out_prob) {
+  constexpr int EPV = Elem<E>::kPerVec;
+  constexpr int VPC = kSampleChunk / EPV;  // 16-byte vectors per chunk
+  constexpr int VPL = VPC / 32;            // per lane
+  constexpr int kWarps = kSampleThreads / 32;
+  __shared__ float s_m[kSampleMaxChunks];
+  __shared__ float s_s[kSampleMaxChunks];
+  __shared__ float s_red[32];
+  __shared__ double s_scan[32];
+  __shared__ int s_chunk, s_tok, s_lastall, s_lastid;
+  __shared__ int s_ri[32];
+  __shared__ double s_target, s_carry, s_total;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int r = blockIdx.x;
+  const E* row = logits + static_cast<int64_t>(r) * stride;
+  const uint4* vp = reinterpret_cast<const uint4*>(row);
+  const int nvec = V / EPV;
+  const int nch = (V + kSampleChunk - 1) / kSampleChunk;
+
+  // 1. Chunks, one warp each at a time (eight vectors per lane in flight).
+  for (int ch = warp; ch < nch; ch += kWarps) {
+    float m = -CUDART_INF_F, sacc = 0.0f;
+#pragma unroll
+    for (int h = 0; h < VPL; h += 8) {
+      uint4 w[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int v = ch * VPC + (h + i) * 32 + lane;
+        w[i] = v < nvec ? ldg_stream(vp + v) : Elem<E>::neg_inf_vec();
+      }
+      float bm = -CUDART_INF_F;
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) bm = fmaxf(bm, Elem<E>::at(w[i], e));
+      if (bm > m) {
+        sacc *= ex2((m - bm) * c);  // m = -inf gives 0
+        m = bm;
+      }
+      if (m > -CUDART_INF_F) {
+        const float mc = m * c;
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+#pragma unroll
+          for (int e = 0; e < EPV; ++e) sacc += ex2(fmaf(Elem<E>::at(w[i], e), c, -mc));
+      }
+    }
+    const float mw = warp_max(m);
+    const float part = m > -CUDART_INF_F ? sacc * ex2((m - mw) * c) : 0.0f;
+    const float sw = warp_sum(part);
+    if (lane == 0) {
+      s_m[ch] = mw;
+      s_s[ch] = sw;
+    }
+  }
+  __syncthreads();
+
+  // 2. The row's maximum, then the chunk that holds u * S (one warp).
+  float mloc = -CUDART_INF_F;
+  for (int ch = tid; ch < nch; ch += kSampleThreads) mloc = fmaxf(mloc, s_m[ch]);
+  const float M = block_max<kSampleThreads>(mloc, s_red);
+  if (warp == 0) {
+    const int per = (nch + 31) / 32;
+    const int q0 = min(nch, lane * per), q1 = min(nch, q0 + per);
+    double sl = 0.0;
+    int lastc = -1;  // the last chunk with a finite logit
+    for (int q = q0; q < q1; ++q) {
+      if (s_m[q] > -CUDART_INF_F) {
+        sl += static_cast<double>(s_s[q]) * static_cast<double>(ex2((s_m[q] - M) * c));
+        lastc = q;
+      }
+    }
+    double incl = sl;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const double y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const double total = __shfl_sync(0xffffffffu, incl, 31);
+    const double target = static_cast<double>(u[r]) * total;
+    const unsigned hb = __ballot_sync(0xffffffffu, sl > 0.0 && incl > target && incl - sl <= target);
+    int chunk = -1;
+    double carry = 0.0;
+    if (hb) {
+      const int wl = __ffs(hb) - 1;
+      if (lane == wl) {
+        double cc = incl - sl;
+        for (int q = q0; q < q1; ++q) {
+          const double s2 =
+              s_m[q] > -CUDART_INF_F ? static_cast<double>(s_s[q]) * static_cast<double>(ex2((s_m[q] - M) * c)) : 0.0;
+          if (s2 > 0.0 && cc + s2 > target) {
+            chunk = q;
+            break;
+          }
+          cc += s2;
+        }
+        carry = cc;
+      }
+      chunk = __shfl_sync(0xffffffffu, chunk, wl);
+      carry = __shfl_sync(0xffffffffu, carry, wl);
+    }
+    lastc = warp_max_i(lastc);
+    if (lane == 0) {
+      s_chunk = chunk;
+      s_carry = carry;
+      s_target = target;
+      s_total = total;
+      s_lastall = lastc;  // the chunk; its last finite id is found below when needed
+      s_lastid = -1;
+      s_tok = INT32_MAX;
+    }
+  }
+  __syncthreads();
+  const int chunk = s_chunk;
+  if (!(s_total > 0.0)) {
+    if (tid == 0) {
+      out_tokens[r] = -1;
+      if (out_prob) out_prob[r] = 0.0f;
+    }
+    return;
+  }
+
+  // 3. The chunk that holds u * S, rescanned: the thread whose ids span it
+  // finds the id.
+  if (chunk >= 0) {
+    const int v = chunk * VPC + tid;
+    float wv[EPV];
+    float mine = 0.0f;
+    if (tid < VPC) {
+      const uint4 w = v < nvec ? __ldcg(vp + v) : Elem<E>::neg_inf_vec();
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) {
+        const float x = Elem<E>::at(w, e);
+        wv[e] = x > -CUDART_INF_F ? ex2((x - M) * c) : 0.0f;
+        mine += wv[e];
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) wv[e] = 0.0f;
+    }
+    double tot;
+    const double excl = block_exclusive_scan_d<kSampleThreads>(static_cast<double>(mine), s_scan, &tot);
+    const double rem = s_target - (s_carry + excl);
+    if (tid < VPC && rem < static_cast<double>(mine)) {
+      const float remf = static_cast<float>(rem);
+      float run = 0.0f;
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) {
+        run += wv[e];
+        if (wv[e] > 0.0f && run > remf) {
+          atomicMin(&s_tok, v * EPV + e);
+          break;
+        }
+      }
+    }
+    __syncthreads();
+  }
+  if (s_tok == INT32_MAX && s_lastall >= 0) {
+    // Rounding left u * S at or past the total: the last id with a finite
+    // logit, in the last chunk that has one.
+    const int v = s_lastall * VPC + tid;
+    int last = -1;
+    if (tid < VPC && v < nvec) {
+      const uint4 w = __ldcg(vp + v);
+#pragma unroll
+      for (int e = 0; e < EPV; ++e)
+        if (Elem<E>::at(w, e) > -CUDART_INF_F) last = v * EPV + e;
+    }
+    last = block_max_i<kSampleThreads>(last, s_ri);
+    if (tid == 0) s_lastid = last;
+    __syncthreads();
+  }
+  if (tid == 0) {
+    const int tok = s_tok != INT32_MAX ? s_tok : s_lastid;
+    if (tok >= 0 && tok < V) {
+      out_tokens[r] = tok;
+      if (out_prob) {
+        const float x = Elem<E>::load(row + tok);
+        out_prob[r] = static_cast<float>(static_cast<double>(ex2((x - M) * c)) / s_total);
+      }
+    } else {
+      out_tokens[r] = -1;
+      if (out_prob) out_prob[r] = 0.0f;
+    }
+  }
+}
+
 sv_status sample_rows(const sv_sample_desc& d, const void* logits, const float* u,
                       int32_t* out_tokens, float* out_prob, void* workspace, cudaStream_t stream) {
   if (d.rows == 0) return SV_OK;
+  {
+    // Without top-p, aligned rows: one pass (sample_stream_kernel).
+    const size_t es = d.dtype == SV_BF16 ? 2 : 4;
+    const int epv = static_cast<int>(16 / es);
+    const bool aligned = (reinterpret_cast<uintptr_t>(logits) & 15u) == 0 && (d.row_stride * es) % 16 == 0 &&
+                         d.vocab % epv == 0;
+    if (d.top_p >= 1.0f && aligned && d.vocab <= kSampleMaxChunks * kSampleChunk) {
+      start_phases(stream);
+      const float c = log2e_over(d.temperature);
+      if (d.dtype == SV_BF16)
+        sample_stream_kernel<uint16_t><<<d.rows, kSampleThreads, 0, stream>>>(
+            static_cast<const uint16_t*>(logits), d.row_stride, d.vocab, c, u, out_tokens, out_prob);
+      else
+        sample_stream_kernel<float><<<d.rows, kSampleThreads, 0, stream>>>(
+            static_cast<const float*>(logits), d.row_stride, d.vocab, c, u, out_tokens, out_prob);
+      if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
+      note_launch(stream);
+      return SV_OK;
+    }
+  }
   RowStats* stats = static_cast<RowStats*>(workspace);
   StatsLaunch L{};
   L.c = log2e_over(d.temperature);
