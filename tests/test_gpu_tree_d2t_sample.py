@@ -177,6 +177,46 @@ def test_build_t2d(sv):
     assert st.item() & 1
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("V", [8, 2048, 4104, 65536])
+def test_sample_rows_one_pass_edge_cases(sv, dtype, V):
+    """The one-pass sampler (no top-p, aligned rows): logits with -inf
+    entries, a row with a single finite logit, an all -inf row (token -1),
+    uniforms 0 and just below 1, rows shorter than one chunk and not a
+    multiple of it."""
+    import torch
+    R = 16
+    g = np.random.default_rng(V)
+    rows = g.normal(0, 2.0, (R, V)).astype(np.float32)
+    rows[g.random((R, V)) < 0.3] = -np.inf
+    rows[1, :] = -np.inf
+    rows[1, V // 3] = 0.5            # a single finite logit
+    rows[2, :] = -np.inf             # no finite logit at all
+    if dtype == "bf16":
+        store = synth.to_bf16_bits(rows)
+        rows = synth.bf16_bits_to_f32(store)
+    else:
+        store = rows
+    u = g.random(R).astype(np.float32)
+    u[3] = 0.0
+    u[4] = np.float32(1.0) - np.float32(2.0 ** -24)
+    tok, prob = sv.sample(logits_tensor(store, dtype), 1.0, 1.0, t(u))
+    torch.cuda.synchronize()
+    tok, prob = tok.cpu().numpy(), prob.cpu().numpy()
+    assert tok[2] == -1 and prob[2] == 0.0
+    assert tok[1] == V // 3 and abs(prob[1] - 1.0) <= 1e-6
+    for r in range(R):
+        if r == 2:
+            continue
+        alts = []
+        want, margin = O.sample_row(rows[r], 1.0, 1.0, float(u[r]), alts=alts)
+        if margin < O.NEAR:
+            continue
+        assert int(tok[r]) == want, (r, int(tok[r]), want, margin)
+        p, _ = O.dist(rows[r], 1.0, 1.0)
+        assert abs(prob[r] - p[want]) <= max(1e-12, 1e-5 * p[want])
+
+
 @pytest.mark.parametrize("dtype,V,top_p", [("f32", 32000, 0.95), ("bf16", 49152, 0.9), ("bf16", 128256, 1.0)])
 def test_sample_rows_full_size(sv, dtype, V, top_p):
     """Draft-side sampling of 1792 rows at once (the qwen3 draft rows'
